@@ -1,0 +1,177 @@
+"""Seeded synthetic inputs for the Grok-1 grouped-query attention core.
+
+This module is the one piece shared by the CPU oracle's tests and by the CUDA
+path's tests and benchmark. It holds shapes, seeds, value distributions and the
+fill pattern of cache slots that no query may read, and none of the method's
+arithmetic: no rotation, no logits, no softmax.
+
+Recipe (the same for every workload): a ``torch.Generator`` seeded with ``seed``
+draws, in this order, ``q [B,T,48,128]``, ``k [B,T,8,128]``, ``v [B,T,8,128]``,
+``cache_k [B,Tmax,8,128]``, ``cache_v [B,Tmax,8,128]`` as ``randn * 3`` in fp32,
+each rounded to bf16 (round to nearest even), then the per-sequence integers
+(start positions for decode, valid lengths for ragged prefill) with
+``torch.randint``. Warm cache rows stand for already-rotated keys. Every cache
+row at or after ``start_pos[b]`` is then overwritten with junk (alternating
++-1e4, or NaN for a poison run): rows ``[start, start+T)`` must be written by the
+append and rows beyond must never be read.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+N_Q_HEADS = 48
+N_KV_HEADS = 8
+HEAD_DIM = 128
+
+JUNK_VALUE = 1.0e4
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic attention workload.
+
+    ``start`` is the per-sequence cache position of the first new token:
+    ``("fixed", n)`` or ``("uniform", lo, hi)`` (inclusive, drawn per sequence).
+    ``valid`` is the per-sequence count of non-padding new tokens:
+    ``("full",)`` or ``("uniform", lo, hi)`` (inclusive).
+    """
+
+    name: str
+    B: int
+    T: int
+    Tmax: int
+    start: tuple
+    valid: tuple
+    description: str
+
+    @property
+    def is_decode(self) -> bool:
+        return self.T == 1
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("prefill_b1_t128", 1, 128, 128, ("fixed", 0), ("full",),
+                 "causal prefill, B=1, T=128, empty cache of 128 rows"),
+        Workload("prefill_b1_t8192", 1, 8192, 8192, ("fixed", 0), ("full",),
+                 "causal prefill, B=1, T=8192, cache of 8192 rows filled by the append"),
+        Workload("decode_b32_ctx8192", 32, 1, 8192, ("uniform", 1, 8191), ("full",),
+                 "one new token per sequence, B=32, cached lengths uniform in [1, 8191]"),
+        Workload("ragged_prefill_b8_t2048", 8, 2048, 2048, ("fixed", 0), ("uniform", 256, 2048),
+                 "causal plus key-padding prefill, B=8, padded T=2048, valid lengths uniform in [256, 2048]"),
+        Workload("chunked_prefill_b4_t256_at6144", 4, 256, 8192, ("fixed", 6144), ("full",),
+                 "256 new tokens at positions 6144..6399 over a warm cache, B=4, Tmax=8192"),
+    )
+}
+
+
+@dataclasses.dataclass
+class Inputs:
+    """Host (CPU) tensors of one workload; bf16 tensors, int32 integer arrays."""
+
+    workload: Workload
+    q: torch.Tensor          # [B, T, 48, 128] bf16
+    k: torch.Tensor          # [B, T, 8, 128] bf16
+    v: torch.Tensor          # [B, T, 8, 128] bf16
+    cache_k: torch.Tensor    # [B, Tmax, 8, 128] bf16
+    cache_v: torch.Tensor    # [B, Tmax, 8, 128] bf16
+    start_pos: torch.Tensor  # [B] int32
+    valid_len: Optional[torch.Tensor]  # [B] int32, or None when every token is valid
+
+    @property
+    def kv_len(self) -> torch.Tensor:
+        """Cache rows in use after the append: start_pos + T."""
+        return (self.start_pos + self.workload.T).to(torch.int32)
+
+
+def _randn_bf16(gen: torch.Generator, shape, scale: float) -> torch.Tensor:
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    x.mul_(scale)
+    return x.to(torch.bfloat16)
+
+
+def _draw(gen: torch.Generator, spec: tuple, B: int) -> torch.Tensor:
+    if spec[0] == "fixed":
+        return torch.full((B,), spec[1], dtype=torch.int32)
+    if spec[0] == "uniform":
+        lo, hi = spec[1], spec[2]
+        return torch.randint(lo, hi + 1, (B,), generator=gen, dtype=torch.int64).to(torch.int32)
+    raise ValueError(f"unknown spec {spec}")
+
+
+def junk_rows_(cache: torch.Tensor, start_pos: torch.Tensor, kind: str = "finite") -> None:
+    """Overwrite rows [start_pos[b], Tmax) of a [B,Tmax,8,128] bf16 cache in place."""
+    if kind == "none":
+        return
+    B, Tmax = cache.shape[0], cache.shape[1]
+    if kind == "finite":
+        pattern = torch.tensor([JUNK_VALUE, -JUNK_VALUE], dtype=torch.float32).to(torch.bfloat16)
+        fill = pattern.repeat(cache.shape[2] * cache.shape[3] // 2).view(cache.shape[2], cache.shape[3])
+    elif kind == "nan":
+        fill = torch.full((cache.shape[2], cache.shape[3]), float("nan"), dtype=torch.bfloat16)
+    else:
+        raise ValueError(kind)
+    for b in range(B):
+        s = int(start_pos[b])
+        if s < Tmax:
+            cache[b, s:] = fill
+
+
+def generate(workload: Workload | str, seed: int = 0, junk: str = "finite",
+             batch: Optional[int] = None, scale: float = 3.0) -> Inputs:
+    """Draw the inputs of ``workload`` (see the module docstring for the recipe).
+
+    ``batch`` overrides B (a smaller batch draws a different, still seeded,
+    sample); ``junk`` is "finite", "nan" or "none".
+    """
+    w = WORKLOADS[workload] if isinstance(workload, str) else workload
+    if batch is not None:
+        w = dataclasses.replace(w, B=batch)
+    B, T, Tmax = w.B, w.T, w.Tmax
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, (B, T, N_Q_HEADS, HEAD_DIM), scale)
+    k = _randn_bf16(gen, (B, T, N_KV_HEADS, HEAD_DIM), scale)
+    v = _randn_bf16(gen, (B, T, N_KV_HEADS, HEAD_DIM), scale)
+    cache_k = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), scale)
+    cache_v = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), scale)
+    start_pos = _draw(gen, w.start, B)
+    valid_len = None if w.valid[0] == "full" else _draw(gen, w.valid, B)
+    if int(start_pos.max()) + T > Tmax:
+        raise ValueError(f"{w.name}: start_pos + T exceeds Tmax")
+    junk_rows_(cache_k, start_pos, junk)
+    junk_rows_(cache_v, start_pos, junk)
+    return Inputs(w, q, k, v, cache_k, cache_v, start_pos, valid_len)
+
+
+def custom(B: int, T: int, Tmax: int, start_pos, valid_len=None, seed: int = 0,
+           junk: str = "finite", scale: float = 3.0) -> Inputs:
+    """Inputs of arbitrary shape with explicit per-sequence integers (edge cases)."""
+    start = torch.as_tensor(np.asarray(start_pos, dtype=np.int32))
+    valid = None if valid_len is None else torch.as_tensor(np.asarray(valid_len, dtype=np.int32))
+    w = Workload(f"custom_b{B}_t{T}_tmax{Tmax}", B, T, Tmax, ("given",), ("given",), "edge case")
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, (B, T, N_Q_HEADS, HEAD_DIM), scale)
+    k = _randn_bf16(gen, (B, T, N_KV_HEADS, HEAD_DIM), scale)
+    v = _randn_bf16(gen, (B, T, N_KV_HEADS, HEAD_DIM), scale)
+    cache_k = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), scale)
+    cache_v = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), scale)
+    junk_rows_(cache_k, start, junk)
+    junk_rows_(cache_v, start, junk)
+    return Inputs(w, q, k, v, cache_k, cache_v, start, valid)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """The raw uint16 storage of a bf16 tensor as a numpy array (no copy of values)."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def from_bits(a: np.ndarray) -> torch.Tensor:
+    """A bf16 tensor whose storage is the given uint16 array."""
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
