@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the Grok-1 GQA attention core on GB300: prints ONE JSON line.
+
+A step is one pass of the prefill hot path over the long causal prefill
+(B=1, T=8192, 48 query / 8 KV heads, d=128, bf16): RoPE + KV-cache append,
+then soft-capped causal GQA attention. `value` is algorithmic attention
+TFLOP/s (48 heads x visible keys x 4 x 128 FLOP per query row) over the whole
+step, inputs resident in HBM. The decode hot path (B=32, cached lengths uniform
+in [1, 8191]: append, split-K decode, combine) is measured in the same run and
+reported under "decode" in KV-cache GB/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (exact fp64 NumPy) on a bounded sample
+of the same workload and metric. Under torchrun (N > 1) each rank runs an
+independent replica (the path shards by sequence and KV head with no
+exchange), times are max-reduced, and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import multiprocessing as mp
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+PREFILL_WORKLOAD = "prefill_b1_t8192"
+DECODE_WORKLOAD = "decode_b32_ctx8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- work counts
+def prefill_flops(start: np.ndarray, valid, T: int) -> float:
+    """48 heads x sum over query rows of visible keys x (2 QK + 2 PV) x 128."""
+    total = 0
+    i = np.arange(T, dtype=np.int64)
+    for b, s in enumerate(start):
+        n = T if valid is None else int(valid[b])
+        total += int((np.minimum(s + i, s + n - 1) + 1).sum())
+    return 48.0 * 4 * 128 * total
+
+
+def decode_bytes(kv_len: np.ndarray) -> float:
+    """K and V rows read once (8 heads x 128 x 2 B each) + q read + out written."""
+    B = len(kv_len)
+    return float(kv_len.astype(np.int64).sum() * 8 * 128 * 2 * 2 + 2 * B * 48 * 128 * 2)
+
+
+def append_bytes(B: int, T: int) -> float:
+    """q, k, v read and q_rot, cache rows written: 2 x B x T x (48 + 8 + 8) x 128 x 2 B."""
+    return 2.0 * B * T * 64 * 128 * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.lines: list[str] = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+_STATE = {}
+
+
+def _oracle_init(name: str):
+    import workloads as W
+    from oracle import rope as R
+    inp = W.generate(name)
+    q_rot, ck, cv = R.rope_kv_append(W.bits(inp.q), W.bits(inp.k), W.bits(inp.v), inp.start_pos.numpy(),
+                                     W.bits(inp.cache_k), W.bits(inp.cache_v))
+    valid = None if inp.valid_len is None else inp.valid_len.numpy()
+    _STATE.update(q_rot=q_rot, ck=ck, cv=cv, start=inp.start_pos.numpy(), valid=valid, T=inp.workload.T)
+
+
+def _oracle_rows(rows):
+    from oracle import attention as A
+    st = _STATE
+    t0 = time.perf_counter()
+    A.attention_rows(st["q_rot"], st["ck"], st["cv"], st["start"], st["valid"], st["T"], rows)
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """The exact fp64 oracle on every host core (spawned workers, one BLAS thread each)."""
+
+    def __init__(self, name: str):
+        import workloads as W
+        self.name = name
+        self.T = W.WORKLOADS[name].T
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_init, initargs=(name,))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def rate(self, n_tokens: int, seed: int):
+        """TFLOP/s of the oracle's attention over n_tokens sampled query tokens x 48 heads.
+
+        Time = the slowest worker's attention time (the workers run concurrently).
+        """
+        rng = np.random.default_rng(seed)
+        toks = np.sort(rng.choice(self.T, size=n_tokens, replace=False))
+        rows = [(0, int(i), h) for i in toks for h in range(48)]
+        chunks = [c for c in (rows[k::self.cores] for k in range(self.cores)) if c]
+        times = self.pool.map(_oracle_rows, chunks)
+        flops = sum(4.0 * 128 * (i + 1) for (_, i, _) in rows)   # empty-cache causal: row i sees i+1 keys
+        return flops / max(times) / 1e12, max(times), len(chunks)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(n_tokens: int = 64) -> dict:
+    pool = OraclePool(PREFILL_WORKLOAD)
+    try:
+        r, wall, used = pool.rate(n_tokens, seed=0)
+    finally:
+        pool.close()
+    return {"value": r, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+            "sample": (f"{n_tokens} random query tokens x 48 heads of {PREFILL_WORKLOAD}, exact fp64 NumPy "
+                       f"oracle, attention only (RoPE/append precomputed), {wall:.1f} s on {used} cores")}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+
+    import grok_gqa_attention_gb300 as G
+    import workloads as W
+    from grok_gqa_attention_gb300 import build as gbuild
+
+    gbuild.build()
+    G.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_kind = load_peaks()
+
+    # ---------------- prefill workload
+    inp = W.generate(PREFILL_WORKLOAD, seed=rank)
+    w = inp.workload
+    B, T, Tmax = w.B, w.T, w.Tmax
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    valid = None if inp.valid_len is None else inp.valid_len.to(dev)
+    q_rot = torch.empty_like(q)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flops = prefill_flops(inp.start_pos.numpy(), None if inp.valid_len is None else inp.valid_len.numpy(), T)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+        if e is not None:
+            e[1].record(stream)
+        G.prefill(q_rot, ck, cv, start, valid, out, status)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    time.sleep(0.5)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms_append = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    ms_prefill = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    if dist:
+        t = torch.tensor([ms, ms_prefill, ms_append], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_prefill, ms_append = (float(x) for x in t.tolist())
+    value = world * flops / (ms * 1e-3) / 1e12
+    prefill_tflops = flops / (ms_prefill * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    result = {
+        "metric": "prefill attention TFLOP/s and decode KV-cache GB/s, % of GB300 roofline",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded randn*3 -> bf16, causal, empty cache)",
+        "config": {"workload": PREFILL_WORKLOAD, "B": B, "T": T, "Tmax": Tmax, "q_heads": 48, "kv_heads": 8,
+                   "head_dim": 128, "algorithmic_gflop_per_step": flops / 1e9,
+                   "l2": "inputs larger than L2 (q, q_rot, out 100 MB each + caches 34 MB)",
+                   "parallelism": f"replicas x{world} (independent sequences, no exchange)"},
+        "kernels_ms": {"rope_kv_append": ms_append, "prefill": ms_prefill},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": prefill_tflops, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": prefill_tflops / peak_tf, "peak_source": f"bf16_tflops ({peak_kind})",
+                     "traffic": None},
+        "append": {"GB/s": append_bytes(B, T) / (ms_append * 1e-3) / 1e9,
+                   "frac_of_hbm": append_bytes(B, T) / (ms_append * 1e-3) / 1e9 / peak_bw},
+        "clocks": clk,
+        "gpu_launches": 2 * args.steps,
+    }
+
+    # ---------------- end to end through the public API with host buffers
+    if not args.no_e2e:
+        qh = inp.q.pin_memory()
+        kh = inp.k.pin_memory()
+        vh = inp.v.pin_memory()
+        sh = inp.start_pos.pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            start.copy_(sh, non_blocking=True)
+            G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+            G.prefill(q_rot, ck, cv, start, valid, out, status)
+            oh.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = a.elapsed_time(b_) / args.steps
+        if dist:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh, sh))
+        result["e2e"] = {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": oh.numel() * oh.element_size()}
+        del qh, kh, vh, oh
+    del q, k, v, ck, cv, q_rot, out
+    torch.cuda.empty_cache()
+
+    # ---------------- decode workload
+    if not args.no_decode:
+        result["decode"] = run_decode(args, rank, world, dist, dev, peaks, peak_kind)
+    return result
+
+
+def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
+    import torch
+
+    import grok_gqa_attention_gb300 as G
+    import workloads as W
+    inp = W.generate(DECODE_WORKLOAD, seed=rank)
+    B, Tmax = inp.workload.B, inp.workload.Tmax
+    n_copies = 3  # rotate independent caches so every step reads from HBM, not L2
+    caches = [(inp.cache_k.to(dev), inp.cache_v.to(dev)) for _ in range(n_copies)]
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    start = inp.start_pos.to(dev)
+    kv_len = (inp.start_pos + 1).to(torch.int32).to(dev)
+    q_rot = torch.empty_like(q)
+    ws = G.alloc_decode_workspace(B, Tmax, dev)
+    out = torch.empty((B, 48, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = decode_bytes((inp.start_pos + 1).numpy())
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(s, e=None):
+        ck, cv = caches[s % n_copies]
+        if e is not None:
+            e[0].record(stream)
+        G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+        if e is not None:
+            e[1].record(stream)
+        G.decode(q_rot[:, 0], ck, cv, kv_len, ws, status)
+        if e is not None:
+            e[2].record(stream)
+        G.combine(ws, kv_len, out, Tmax, status)
+        if e is not None:
+            e[3].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    if dist:
+        dist.barrier()
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(args.steps):
+        step(s, ev[s])
+    b_.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b_) / args.steps
+    ms_dec = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    ms_comb = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+    ms_app = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    if dist:
+        t = torch.tensor([ms, ms_dec], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_dec = (float(x) for x in t.tolist())
+    peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs_step = world * nbytes / (ms * 1e-3) / 1e9
+    gbs_kernel = nbytes / (ms_dec * 1e-3) / 1e9
+    return {
+        "workload": DECODE_WORKLOAD, "value": gbs_step, "unit": "GB/s", "ms_per_step": ms,
+        "algorithmic_bytes_per_step": nbytes,
+        "kernels_ms": {"rope_kv_append": ms_app, "decode": ms_dec, "combine": ms_comb},
+        "l2": f"{n_copies} rotating cache copies of {nbytes / 1e6:.0f} MB used rows each",
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs_kernel, "peak": peak_bw,
+                     "unit": "GB/s", "frac": gbs_kernel / peak_bw, "peak_source": f"hbm_gbs ({peak_kind})",
+                     "traffic": None},
+        "gpu_launches": 3 * args.steps,
+    }
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on a bounded sample of the prefill workload per step."""
+    pool = OraclePool(PREFILL_WORKLOAD)
+    n_tokens = 8
+    try:
+        rates, walls = [], []
+        for s in range(args.steps):
+            r, wall, cores = pool.rate(n_tokens, seed=1000 + s)
+            rates.append(r)
+            walls.append(wall)
+    finally:
+        pool.close()
+    value = float(np.mean(rates))
+    sample = (f"per step {n_tokens} random query tokens x 48 heads of {PREFILL_WORKLOAD}, exact fp64 NumPy oracle, "
+              f"attention only (RoPE/append precomputed once)")
+    return {
+        "impl": "reference",
+        "metric": "prefill attention TFLOP/s and decode KV-cache GB/s, % of GB300 roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": float(np.mean(walls)) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn*3 -> bf16, causal, empty cache)",
+        "config": {"workload": PREFILL_WORKLOAD, "B": 1, "T": 8192, "Tmax": 8192},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()   # before any GPU work; the pool is spawned, never forked
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+"""Python binding of libgrok_attn.so, the GB300 Grok-1 GQA attention core.
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their dtype, shape and layout, and passes raw pointers and sizes to the C ABI
+declared in include/grok_attn.h. All arithmetic runs in the library's CUDA
+kernels; there is no other code path, and every call raises if the library is
+not built or the device is not an sm_103 GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+N_Q_HEADS = 48
+N_KV_HEADS = 8
+HEAD_DIM = 128
+DECODE_SPLIT = 512
+MAX_POSITION = 65536
+
+DEV_BAD_START = 0x1
+DEV_BAD_VALID = 0x2
+DEV_BAD_KV_LEN = 0x4
+DEV_TIMEOUT = 0x8
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgrok_attn.so")
+
+EXPORTS = (
+    "grok_abi_version",
+    "grok_last_error",
+    "grok_rope_kv_append",
+    "grok_attn_prefill",
+    "grok_attn_decode_workspace",
+    "grok_attn_decode",
+    "grok_attn_combine",
+)
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class GrokError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"grok status {status}: {message}")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with grok_gqa_attention_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.grok_abi_version.restype = I
+    lib.grok_abi_version.argtypes = []
+    lib.grok_last_error.restype = ctypes.c_char_p
+    lib.grok_last_error.argtypes = []
+    lib.grok_rope_kv_append.restype = I
+    lib.grok_rope_kv_append.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P]
+    lib.grok_attn_prefill.restype = I
+    lib.grok_attn_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
+    lib.grok_attn_decode_workspace.restype = I
+    lib.grok_attn_decode_workspace.argtypes = [I, I, ctypes.POINTER(S), ctypes.POINTER(I)]
+    lib.grok_attn_decode.restype = I
+    lib.grok_attn_decode.argtypes = [P, P, P, P, I, I, P, S, P, P]
+    lib.grok_attn_combine.restype = I
+    lib.grok_attn_combine.argtypes = [P, S, P, I, I, P, P, P]
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load().grok_last_error()
+        raise GrokError(status, msg.decode() if msg else "")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _want(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def abi_version() -> int:
+    return load().grok_abi_version()
+
+
+def rope_kv_append(q, k, v, start_pos, q_rot, cache_k, cache_v, dev_status=None, stream=None) -> None:
+    """RoPE on q and k; rotated k and raw v written to the caches at start_pos[b] (in place)."""
+    B, T = q.shape[0], q.shape[1]
+    Tmax = cache_k.shape[1]
+    _want(q, "q", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(k, "k", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(v, "v", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_rope_kv_append(_ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), B, T, Tmax, _ptr(q_rot),
+                                      _ptr(cache_k), _ptr(cache_v), _ptr(dev_status), _stream(stream)))
+
+
+def prefill(q_rot, cache_k, cache_v, start_pos, valid_len, out, dev_status=None, stream=None) -> None:
+    """Soft-capped causal GQA attention of T new tokens over the cache (valid_len may be None)."""
+    B, T = q_rot.shape[0], q_rot.shape[1]
+    Tmax = cache_k.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    if valid_len is not None:
+        _want(valid_len, "valid_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_attn_prefill(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(start_pos), _ptr(valid_len),
+                                    B, T, Tmax, _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def decode_workspace(B: int, Tmax: int) -> tuple[int, int]:
+    """(bytes, splits per sequence) of the workspace decode() needs."""
+    n = ctypes.c_size_t(0)
+    s = ctypes.c_int(0)
+    _check(load().grok_attn_decode_workspace(B, Tmax, ctypes.byref(n), ctypes.byref(s)))
+    return n.value, s.value
+
+
+def alloc_decode_workspace(B: int, Tmax: int, device=None) -> torch.Tensor:
+    """A caller-owned workspace tensor for decode()/combine() (256-byte aligned by torch)."""
+    nbytes, _ = decode_workspace(B, Tmax)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode(q_rot, cache_k, cache_v, kv_len, workspace, dev_status=None, stream=None) -> None:
+    """Split-K part of a decode step: per-split partial sums into the workspace."""
+    B, Tmax = cache_k.shape[0], cache_k.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(kv_len, "kv_len", torch.int32, (B,))
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().grok_attn_decode(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(kv_len), B, Tmax,
+                                   _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
+
+
+def combine(workspace, kv_len, out, Tmax: int, dev_status=None, stream=None) -> None:
+    """Combine part of a decode step: out[b, h] = sum of split partials / sum of split row sums."""
+    B = out.shape[0]
+    _want(kv_len, "kv_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().grok_attn_combine(_ptr(workspace), nbytes, _ptr(kv_len), B, Tmax, _ptr(out),
+                                    _ptr(dev_status), _stream(stream)))
+
+
+def decode_step(q_rot, cache_k, cache_v, kv_len, workspace, out, dev_status=None, stream=None) -> None:
+    """decode() then combine() on the same stream."""
+    decode(q_rot, cache_k, cache_v, kv_len, workspace, dev_status, stream)
+    combine(workspace, kv_len, out, cache_k.shape[1], dev_status, stream)

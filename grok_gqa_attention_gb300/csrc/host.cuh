@@ -1,0 +1,30 @@
+// Host-side helpers shared by the entry points: thread-local error text,
+// argument checks, device capability and TMA tensor-map encoding.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "grok_attn.h"
+
+namespace grok {
+
+// Record a message for grok_last_error() and return `s`.
+grok_status fail(grok_status s, const char* fmt, ...);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The current device must be compute capability 10.3; returns its SM count.
+grok_status device_sm_count(int* sm_count);
+
+// Launch-error check after a kernel launch.
+grok_status check_launch(const char* what);
+
+// 4-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+// dims innermost first; strides in bytes for dims 1..3.
+grok_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                                const uint64_t strides[3], const uint32_t box[4]);
+
+}  // namespace grok

@@ -1,0 +1,413 @@
+// K2: prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Grok-1 code-reading guide, ch. 4 "model.py close reading I": §4.5.2 (GQA
+// logits, query head h reads KV head h / 6, multiplier 1/sqrt(128), soft cap
+// 30 tanh(x / 30)), §4.5.3 (mask, softmax over keys in fp32), §4.5.4 (weighted
+// sum of V); ch. 6 "model.py close reading II", §6.4.2 (causal x padding mask).
+//
+// Work item = (sequence b, 128-row query tile, KV group g, pair of query heads
+// of that group). One persistent CTA per SM walks the items, heaviest first.
+// Both heads of an item read the same K/V tiles, so every K/V tile staged in
+// shared memory by TMA feeds two heads; the three head pairs of a group run in
+// neighbouring CTAs and meet the same tiles in L2.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles of both heads, then K/V tiles (2 stages)
+//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warps 4-7   softmax + epilogue for head slot 0 (TMEM lanes 0..127)
+//   warps 8-11  softmax + epilogue for head slot 1
+// TMEM (512 columns): per slot, S = Q K^T in 128 fp32 columns and O in 128.
+// The softmax warps overwrite S in place with P as two bf16 halves (hi, lo)
+// that sum to P to ~2^-16; O += P_hi V + P_lo V reads them straight from TMEM.
+//
+// Softmax without a running maximum: every capped logit is below 30, so the
+// weights exp(c - 30) lie in (e^-60, 1] and fp32 holds them and their sums
+// with full relative precision. O therefore accumulates across all key tiles
+// with no rescaling; the epilogue divides by the row sum once.
+//
+// Keys beyond the last visible row of an item's final tile may hold anything
+// (including NaN): the softmax gives them weight 0 by selection and the slot-0
+// warps zero those rows of the staged V tile before the PV product reads it.
+#include "common.cuh"
+#include "host.cuh"
+
+namespace grok {
+
+constexpr int kPfThreads = 384;
+constexpr int kPfRows = 128;   // query rows per tile (MMA M)
+constexpr int kPfKeys = 128;   // keys per K/V tile (MMA N for Q K^T, K for P V)
+constexpr int kPfStages = 2;
+constexpr int kBox = 128 * 128;             // [128 rows][64 bf16], 128-byte swizzled
+constexpr int kQBytes = 2 * 2 * kBox;       // two heads, two 64-wide halves of d
+constexpr int kKVBytes = 4 * kBox;          // K halves then V halves
+constexpr int kPfData = kQBytes + kPfStages * kKVBytes;
+
+struct PfBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kPfStages], kv_empty[kPfStages];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kPfSmem = kPfData + int(sizeof(PfBars)) + 1024;
+
+struct PfParams {
+  int B, T, Tmax, n_qt, n_items;
+  const int32_t* start_pos;
+  const int32_t* valid_len;
+  uint4* out;
+  int32_t* status;
+};
+
+struct PfItem {
+  int b, qt, g, hp;
+  int s, n;     // start position, valid length
+  int kv_end;   // keys [0, kv_end) are visible to some row of the tile
+  int n_kv;     // key tiles to visit (0: skip the item)
+  int bad;      // GROK_DEV_* bits when the sequence's integers are invalid
+};
+
+__device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
+  PfItem it;
+  it.hp = item % 3;
+  int rest = item / 3;
+  it.g = rest % kKVHeads;
+  rest /= kKVHeads;
+  it.b = rest % p.B;
+  it.qt = p.n_qt - 1 - rest / p.B;  // heaviest (last) query tiles first
+  it.s = __ldg(p.start_pos + it.b);
+  it.n = p.valid_len ? __ldg(p.valid_len + it.b) : p.T;
+  it.bad = 0;
+  if (it.s < 0 || (long long)it.s + p.T > p.Tmax) it.bad |= GROK_DEV_BAD_START;
+  if (it.n < 1 || it.n > p.T) it.bad |= GROK_DEV_BAD_VALID;
+  if (it.bad) {
+    it.kv_end = 0;
+    it.n_kv = 0;
+    return it;
+  }
+  const int last_row = min(it.qt * kPfRows + kPfRows, p.T);  // rows [qt*128, last_row)
+  it.kv_end = min(it.s + last_row, it.s + it.n);
+  it.n_kv = (it.kv_end + kPfKeys - 1) / kPfKeys;
+  return it;
+}
+
+__device__ __forceinline__ void pf_issue_qk(uint32_t tmem, int slot, uint32_t sq, uint32_t skv) {
+  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kPfKeys, 0);
+  const uint32_t a0 = sq + slot * 2 * kBox;
+  const uint32_t d = tmem + slot * 256;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {  // K = 128 in steps of 16
+    const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+    umma_ss(d, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(skv + off, 16, 1024), idesc, kk > 0);
+  }
+}
+
+__device__ __forceinline__ void pf_issue_pv(uint32_t tmem, int slot, uint32_t skv, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kD, 1);  // V is N(d)-contiguous
+  const uint32_t v0 = skv + 2 * kBox;
+  const uint32_t d = tmem + slot * 256 + 128;
+  const uint32_t pbase = tmem + slot * 256;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
+    // P for keys 32c..32c+31: hi in columns 32c..32c+15, lo in 32c+16..32c+31
+    const uint32_t pcol = (kk >> 1) * 32 + (kk & 1) * 8;
+    const uint64_t bdesc = make_sdesc_sw128(v0 + kk * 2048, kBox, 1024);
+    umma_ts(d, pbase + pcol, bdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(d, pbase + pcol + 16, bdesc, idesc, 1u);
+  }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQBytes;
+  PfBars* bars = reinterpret_cast<PfBars*>(smem + kPfData);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->o_full[s], 1);
+      mbar_init(&bars->o_empty[s], 128);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int kv_it = 0, q_it = 0;
+      for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const PfItem it = pf_item(p, item);
+        if (it.n_kv == 0) continue;
+        if (!mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort, p.status)) break;
+        mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+        for (int hs = 0; hs < 2; ++hs) {
+          const int h = it.g * kGroup + it.hp * 2 + hs;
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(sQ + (hs * 2 + half) * kBox, &tm_q, &bars->q_full, half * 64, h, it.qt * kPfRows, it.b);
+        }
+        ++q_it;
+        bool ok = true;
+        for (int j = 0; j < it.n_kv; ++j, ++kv_it) {
+          const int st = kv_it % kPfStages;
+          if (!mbar_wait(&bars->kv_empty[st], ((kv_it / kPfStages) & 1) ^ 1, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->kv_full[st], kKVBytes);
+          uint8_t* base = sKV + st * kKVBytes;
+          tma_load_4d(base, &tm_k, &bars->kv_full[st], 0, it.g, j * kPfKeys, it.b);
+          tma_load_4d(base + kBox, &tm_k, &bars->kv_full[st], 64, it.g, j * kPfKeys, it.b);
+          tma_load_4d(base + 2 * kBox, &tm_v, &bars->kv_full[st], 0, it.g, j * kPfKeys, it.b);
+          tma_load_4d(base + 3 * kBox, &tm_v, &bars->kv_full[st], 64, it.g, j * kPfKeys, it.b);
+        }
+        if (!ok) break;
+      }
+      // Drain: copies still in flight (only after an abort) land before the CTA exits.
+      volatile int never = 0;
+      for (int t = max(0, kv_it - kPfStages); t < kv_it; ++t)
+        mbar_wait(&bars->kv_full[t % kPfStages], (t / kPfStages) & 1, &never, p.status);
+      if (q_it > 0) mbar_wait(&bars->q_full, (q_it - 1) & 1, &never, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(sQ), skv0 = smem_u32(sKV);
+      int kv_it = 0, q_it = 0, item_it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        const PfItem it = pf_item(p, item);
+        if (it.n_kv == 0) continue;
+        if (!mbar_wait(&bars->q_full, q_it & 1, abort, p.status)) break;
+        {
+          const int st = kv_it % kPfStages;
+          if (!mbar_wait(&bars->kv_full[st], (kv_it / kPfStages) & 1, abort, p.status)) break;
+          tc_fence_after();
+          for (int slot = 0; slot < 2; ++slot) {
+            pf_issue_qk(tmem, slot, sq, skv0 + st * kKVBytes);
+            umma_commit(&bars->s_full[slot]);
+          }
+        }
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          const int cur = kv_it + j;
+          const int st = cur % kPfStages;
+          const bool has_next = j + 1 < it.n_kv;
+          const int stn = (cur + 1) % kPfStages;
+          if (has_next) {
+            if (!mbar_wait(&bars->kv_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+          }
+          for (int slot = 0; slot < 2; ++slot) {
+            if (!mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            if (j == 0 && !mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pf_issue_pv(tmem, slot, skv0 + st * kKVBytes, j > 0);
+            if (has_next) {
+              pf_issue_qk(tmem, slot, sq, skv0 + stn * kKVBytes);
+              umma_commit(&bars->s_full[slot]);
+            } else {
+              umma_commit(&bars->o_full[slot]);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&bars->kv_empty[st]);
+          if (!has_next) umma_commit(&bars->q_empty);
+        }
+        kv_it += it.n_kv;
+        ++q_it;
+        ++item_it;
+      }
+      // No MMA may still be running when TMEM is released.
+      umma_commit(&bars->mma_done);
+      volatile int never = 0;
+      mbar_wait(&bars->mma_done, 0, &never, p.status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int slot = (warp - 4) >> 2;
+    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;            // query row within the tile
+    const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
+    int tile_cnt = 0, item_it = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+      const PfItem it = pf_item(p, item);
+      if (it.n_kv == 0) {
+        if (it.bad && slot == 0 && r == 0) report(p.status, it.bad);
+        continue;
+      }
+      const int i = it.qt * kPfRows + r;
+      const int lim = min(it.s + i, it.s + it.n - 1);  // last visible key of this row
+      float l0 = 0.f, l1 = 0.f;
+      bool ok = true;
+      for (int j = 0; j < it.n_kv; ++j) {
+        if (!mbar_wait(&bars->s_full[slot], (tile_cnt + j) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int rel = lim - j * kPfKeys;       // columns c <= rel are visible
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {            // 32 keys at a time
+          uint32_t sv[32];
+          tmem_ld32(trow + c * 32, sv);
+          tmem_wait_ld();
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float w0 = capped_weight(__uint_as_float(sv[2 * e]));
+            float w1 = capped_weight(__uint_as_float(sv[2 * e + 1]));
+            w0 = (c * 32 + 2 * e <= rel) ? w0 : 0.f;
+            w1 = (c * 32 + 2 * e + 1 <= rel) ? w1 : 0.f;
+            l0 += w0;
+            l1 += w1;
+            split_bf16x2(w0, w1, hi[e], lo[e]);
+          }
+          tmem_st16(trow + c * 32, hi);
+          tmem_st16(trow + c * 32 + 16, lo);
+        }
+        if (slot == 0 && j == it.n_kv - 1) {
+          // Zero the V rows of the last tile that lie beyond every visible key.
+          const int first_dead = it.kv_end - j * kPfKeys;
+          if (r >= first_dead) {
+            const int st = (tile_cnt + j) % kPfStages;
+            uint4* v0 = reinterpret_cast<uint4*>(sKV + st * kKVBytes + 2 * kBox + r * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(sKV + st * kKVBytes + 3 * kBox + r * 128);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              v0[q] = z;
+              v1[q] = z;
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[slot]);
+      }
+      if (!ok) break;
+      tile_cnt += it.n_kv;
+      // epilogue: O / l -> bf16
+      if (!mbar_wait(&bars->o_full[slot], item_it & 1, abort, p.status)) break;
+      tc_fence_after();
+      const float inv_l = 1.0f / (l0 + l1);
+      const int h = it.g * kGroup + it.hp * 2 + slot;
+      uint4* dst = p.out + (((size_t)it.b * p.T + i) * kQHeads + h) * 16;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(trow + 128 + c * 32, ov);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        if (i < p.T) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[c * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty[slot]);
+      ++item_it;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace grok
+
+using namespace grok;
+
+extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k,
+                                         const grok_bf16* cache_v, const int32_t* start_pos,
+                                         const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
+                                         int32_t* dev_status, void* stream) {
+  if (!q_rot || !cache_k || !cache_v || !start_pos || !out)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: null pointer");
+  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: bf16 tensors must be 16-byte aligned");
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+                GROK_MAX_POSITION, B, T, Tmax);
+  int sms = 0;
+  grok_status st = device_sm_count(&sms);
+  if (st != GROK_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  const uint32_t box[4] = {64, 1, 128, 1};
+  {
+    const uint64_t dims[4] = {kD, kQHeads, uint64_t(T), uint64_t(B)};
+    const uint64_t strides[3] = {kD * 2, uint64_t(kQHeads) * kD * 2, uint64_t(T) * kQHeads * kD * 2};
+    if ((st = encode_tmap_bf16_4d(&tq, q_rot, dims, strides, box)) != GROK_OK) return st;
+  }
+  {
+    const uint64_t dims[4] = {kD, kKVHeads, uint64_t(Tmax), uint64_t(B)};
+    const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, uint64_t(Tmax) * kKVHeads * kD * 2};
+    if ((st = encode_tmap_bf16_4d(&tk, cache_k, dims, strides, box)) != GROK_OK) return st;
+    if ((st = encode_tmap_bf16_4d(&tv, cache_v, dims, strides, box)) != GROK_OK) return st;
+  }
+  PfParams prm;
+  prm.B = B;
+  prm.T = T;
+  prm.Tmax = Tmax;
+  prm.n_qt = (T + kPfRows - 1) / kPfRows;
+  prm.n_items = prm.n_qt * B * kKVHeads * 3;
+  prm.start_pos = start_pos;
+  prm.valid_len = valid_len;
+  prm.out = reinterpret_cast<uint4*>(out);
+  prm.status = dev_status;
+
+  static bool attr_set = false;  // idempotent: every thread would set the same value
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    attr_set = true;
+  }
+  const int grid = prm.n_items < sms ? prm.n_items : sms;
+  prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, prm);
+  return check_launch("prefill");
+}

@@ -1,0 +1,152 @@
+/*
+ * grok_attn.h - C ABI of the GB300 (sm_103a) Grok-1 grouped-query attention core.
+ *
+ * The operation is the self-attention core of Grok-1 as quoted in the Grok-1
+ * code-reading guide (yingwang.github.io/grok-1/):
+ *   ch. 4 "model.py close reading I: RMSNorm, RoPE, GQA Attention"
+ *     §4.3 / §4.3.1  rotate_half and RotaryEmbedding (RoPE, base 10000, NeoX pairing)
+ *     §4.4           RoPE on K and Q before the KV-cache write; update_into; memory mask
+ *     §4.5.2         GQA: 48 query heads, 8 KV heads, query head h uses KV head h / 6;
+ *                    logits * attn_output_multiplier (1/sqrt(128)); 30 * tanh(x / 30)
+ *     §4.5.3         where(mask, logits, -1e30); softmax over keys in fp32
+ *     §4.5.4         weighted sum of V, heads flattened in order h = 6 g + r
+ *   ch. 6 "model.py close reading II"
+ *     §6.4.2         causal (tril) x key-padding mask; decode masks through the memory mask
+ *     §6.6 / §6.6.1  KVMemory(k, v, step): caches [B, Tmax, 8, 128] bf16, per-sequence step
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as grok_bf16 (uint16_t storage), row-major with the
+ *     innermost dimension contiguous and no padding:
+ *       q, q_rot, out  [B, T, 48, 128]      k, v  [B, T, 8, 128]
+ *       cache_k/v      [B, Tmax, 8, 128]
+ *   - every pointer argument is a DEVICE pointer owned by the caller; the
+ *     library never allocates, frees or retains caller memory, and every
+ *     pointer to a bf16 tensor must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every call
+ *     is asynchronous on it and returns after enqueueing its kernels.
+ *   - errors found on the host (null or misaligned pointers, bad sizes) return
+ *     GROK_ERR_INVALID_ARG before anything is launched; a failed launch returns
+ *     GROK_ERR_CUDA. grok_last_error() then describes it (thread-local).
+ *   - errors that depend on device data (positions, lengths) or a bounded wait
+ *     that gave up are OR-ed into *dev_status (a device int32 the caller zeroes;
+ *     NULL disables reporting) as GROK_DEV_* bits. The kernels never trap or
+ *     hang; a sequence whose integers are invalid is skipped (its outputs and
+ *     cache rows are left untouched).
+ *   - positions must stay below GROK_MAX_POSITION (the fp32 RoPE chain is exact
+ *     and bit-reproducible there).
+ */
+#ifndef GROK_ATTN_H
+#define GROK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GROK_ATTN_ABI_VERSION 1
+
+#define GROK_N_Q_HEADS 48
+#define GROK_N_KV_HEADS 8
+#define GROK_HEAD_DIM 128
+#define GROK_MAX_POSITION 65536
+/* keys per decode split (one partial result per split) */
+#define GROK_DECODE_SPLIT 512
+
+typedef uint16_t grok_bf16;
+
+typedef enum {
+  GROK_OK = 0,
+  GROK_ERR_INVALID_ARG = 1,
+  GROK_ERR_UNSUPPORTED = 2, /* no sm_103 device, or a size this build does not cover */
+  GROK_ERR_CUDA = 3         /* a CUDA runtime or driver call failed */
+} grok_status;
+
+/* bits OR-ed into *dev_status by the kernels */
+#define GROK_DEV_BAD_START 0x1   /* start_pos[b] < 0, start_pos[b] + T > Tmax, or > GROK_MAX_POSITION */
+#define GROK_DEV_BAD_VALID 0x2   /* valid_len[b] outside [1, T] */
+#define GROK_DEV_BAD_KV_LEN 0x4  /* kv_len[b] outside [1, Tmax] */
+#define GROK_DEV_TIMEOUT 0x8     /* a bounded wait inside a kernel gave up */
+
+/* ABI version this library was built with (GROK_ATTN_ABI_VERSION). */
+int grok_abi_version(void);
+
+/* Message describing the last non-OK status returned on this thread. */
+const char* grok_last_error(void);
+
+/*
+ * RoPE on Q and K, then the KV-cache append (ch. 4 §4.3.1, §4.4).
+ *
+ * For sequence b and new token i (position p = start_pos[b] + i), every query
+ * head and every KV head is rotated pairwise (feature j with feature j + 64):
+ *   inv_freq[j] = 1 / RN32(10000^(j/64)),  phase = RN32(p * inv_freq[j]),
+ *   c = RN32(cos(phase)), s = RN32(sin(phase)) (fp64 evaluation),
+ *   x'[j] = RN32(RN32(x[j] c) - RN32(x[j+64] s)),
+ *   x'[j+64] = RN32(RN32(x[j+64] c) + RN32(x[j] s)), rounded to bf16 (nearest even).
+ * Rotated Q goes to q_rot; rotated K and raw V are written to cache rows
+ * [start_pos[b], start_pos[b] + T) of sequence b; no other cache row is touched.
+ *   q [B,T,48,128], k, v [B,T,8,128] in; start_pos [B] int32 (device);
+ *   q_rot [B,T,48,128] out (may not alias q); cache_k, cache_v [B,Tmax,8,128] in/out.
+ * The caller advances its step counter by T afterwards (new_step = step + T).
+ */
+grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                const int32_t* start_pos, int B, int T, int Tmax, grok_bf16* q_rot,
+                                grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status, void* stream);
+
+/*
+ * Prefill attention of T new tokens per sequence over the appended cache
+ * (ch. 4 §4.5.2-§4.5.4, ch. 6 §6.4.2).
+ *
+ * Query i of sequence b (cache position start_pos[b] + i) attends cache row j iff
+ *   j <= start_pos[b] + i  and  j < start_pos[b] + valid_len[b];
+ * logits = (q_rot . k) / sqrt(128), capped as 30 tanh(x / 30), softmax over the
+ * visible rows, output = sum of weights x v, rounded to bf16. Padding query rows
+ * (i >= valid_len[b]) are computed too. Query head h reads KV head h / 6.
+ *   q_rot [B,T,48,128]; cache_k, cache_v [B,Tmax,8,128]; start_pos [B] int32;
+ *   valid_len [B] int32 or NULL (= T for every sequence); out [B,T,48,128].
+ * Requires T <= Tmax and T, Tmax >= 1.
+ */
+grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
+                              const int32_t* start_pos, const int32_t* valid_len, int B, int T, int Tmax,
+                              grok_bf16* out, int32_t* dev_status, void* stream);
+
+/*
+ * Bytes of device workspace grok_attn_decode needs for B sequences and a cache
+ * of Tmax rows (fp32 partial sums per split of GROK_DECODE_SPLIT keys), and the
+ * number of splits per sequence. Either output pointer may be NULL.
+ */
+grok_status grok_attn_decode_workspace(int B, int Tmax, size_t* bytes, int* max_splits);
+
+/*
+ * One decode step, split-K part (ch. 4 §4.4.1; ch. 6 §6.4.2: the new token
+ * attends every cache row below step + 1, which the memory mask selects).
+ *
+ * For sequence b the single query q_rot[b] (its own K/V already appended at
+ * row kv_len[b] - 1) is scored against cache rows [0, kv_len[b]) in splits of
+ * GROK_DECODE_SPLIT rows. Each split writes, per query head, the sums
+ *   l = sum_j exp(c_j - 30),  o = sum_j exp(c_j - 30) v_j
+ * (c = capped logit; 30 bounds every capped logit, so no running maximum is
+ * needed) into `workspace`. grok_attn_combine finishes the step.
+ *   q_rot [B,48,128]; cache_k, cache_v [B,Tmax,8,128]; kv_len [B] int32 (device);
+ *   workspace: device buffer of at least grok_attn_decode_workspace bytes,
+ *   256-byte aligned, owned by the caller.
+ */
+grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
+                             const int32_t* kv_len, int B, int Tmax, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * Decode step, combine part: out[b, h] = (sum over splits of o) / (sum over
+ * splits of l), rounded to bf16. Reads the workspace written by
+ * grok_attn_decode with the same B, Tmax and kv_len.
+ *   out [B,48,128] bf16.
+ */
+grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len, int B,
+                              int Tmax, grok_bf16* out, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GROK_ATTN_H */

@@ -1,0 +1,68 @@
+"""K1 parity: rotated Q and the appended KV cache must equal the oracle bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_util import cached_inputs, oracle_append, run_append
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_append_bit_exact_at_full_size(name):
+    inp = cached_inputs(name)
+    q_rot, ck, cv, status = run_append(inp)
+    assert status == 0
+    oq, ok_, ov = oracle_append(inp)
+    assert np.array_equal(W.bits(q_rot.cpu()), oq)
+    assert np.array_equal(W.bits(ck.cpu()), ok_)   # written rows and untouched rows
+    assert np.array_equal(W.bits(cv.cpu()), ov)
+
+
+def test_append_positions_spread_over_supported_range():
+    starts = [b * 4096 + (b * 37) % 256 for b in range(15)] + [65536 - 256]
+    inp = W.custom(B=16, T=256, Tmax=65536, start_pos=starts, seed=3)
+    q_rot, ck, cv, status = run_append(inp)
+    assert status == 0
+    oq, ok_, ov = oracle_append(inp)
+    assert np.array_equal(W.bits(q_rot.cpu()), oq)
+    assert np.array_equal(W.bits(ck.cpu()), ok_)
+    assert np.array_equal(W.bits(cv.cpu()), ov)
+
+
+def test_append_ragged_token_counts():
+    for T in (1, 3, 129):
+        inp = W.custom(B=3, T=T, Tmax=300, start_pos=[0, 7, 300 - T], seed=T)
+        q_rot, ck, cv, status = run_append(inp)
+        assert status == 0
+        oq, ok_, ov = oracle_append(inp)
+        assert np.array_equal(W.bits(q_rot.cpu()), oq)
+        assert np.array_equal(W.bits(ck.cpu()), ok_)
+        assert np.array_equal(W.bits(cv.cpu()), ov)
+
+
+def test_append_invalid_start_sets_status_and_skips_sequence():
+    import grok_gqa_attention_gb300 as G
+    inp = W.custom(B=2, T=8, Tmax=16, start_pos=[4, 9], seed=5)   # 9 + 8 > 16
+    q_rot, ck, cv, status = run_append(inp)
+    assert status & G.DEV_BAD_START
+    oq, ok_, ov = oracle_append(W.custom(B=2, T=8, Tmax=16, start_pos=[4, 0], seed=5))
+    assert np.array_equal(W.bits(ck.cpu())[0], ok_[0])
+    assert np.array_equal(W.bits(ck.cpu())[1], W.bits(inp.cache_k)[1])   # untouched
+    assert np.array_equal(W.bits(cv.cpu())[1], W.bits(inp.cache_v)[1])
+
+
+def test_append_host_argument_checks():
+    import grok_gqa_attention_gb300 as G
+    inp = W.custom(B=1, T=4, Tmax=8, start_pos=[0], seed=6)
+    dev = "cuda"
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    with pytest.raises(G.GrokError):          # q_rot aliasing q is rejected by the library
+        G.rope_kv_append(q, k, v, start, q, ck, cv)
+    flat = torch.empty(q.numel() + 1, dtype=torch.bfloat16, device=dev)
+    mis = flat[1:].view(q.shape)              # 2-byte offset: not 16-byte aligned
+    with pytest.raises(G.GrokError):
+        G.rope_kv_append(q, k, v, start, mis, ck, cv)
