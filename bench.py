@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one workload only (profiling); implies --no-cpu-baseline --no-e2e")
     return ap.parse_args()
 
 
@@ -354,7 +356,7 @@ def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
     import workloads as W
     inp = W.generate(DECODE_WORKLOAD, seed=rank)
     B, Tmax = inp.workload.B, inp.workload.Tmax
-    n_copies = 3  # rotate independent caches so every step reads from HBM, not L2
+    n_copies = 1 if args.only else 3  # rotate independent caches so every step reads from HBM, not L2
     caches = [(inp.cache_k.to(dev), inp.cache_v.to(dev)) for _ in range(n_copies)]
     q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
     start = inp.start_pos.to(dev)
@@ -448,6 +450,10 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.only:
+        args.no_cpu_baseline = True
+        args.no_e2e = True
+        args.no_decode = args.only == "prefill"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int key = key_base + 8 * n + 2 * t4 + e;
-          const float x = capped_weight(s[n][e]);
+          const float x = capped_weight_precise(s[n][e]);
           w[n][e] = (qrow < kGroup && key < k1) ? x : 0.f;
           lsum += w[n][e];
         }

@@ -11,11 +11,23 @@
 // shared memory by TMA feeds two heads; the three head pairs of a group run in
 // neighbouring CTAs and meet the same tiles in L2.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA producer: Q tiles of both heads, then K/V tiles (2 stages)
-//   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 4-7   softmax + epilogue for head slot 0 (TMEM lanes 0..127)
-//   warps 8-11  softmax + epilogue for head slot 1
+// Warp roles (608 threads):
+//   warp 0      TMA producer: Q tiles of both heads, then K and V tiles in two
+//               separate 2-stage rings (a K tile is released as soon as both
+//               heads' Q K^T products finish, a tile ahead of its V tile)
+//   warp 1      TMEM owner and MMA issuer of head slot 0 (one thread)
+//   warp 18     MMA issuer of head slot 1 (one thread, on another SMSP). The
+//               two issuers pass a token so the tensor queue alternates
+//               slot 0 / slot 1 per key tile (one slot's softmax then overlaps
+//               the other's products), while each issuer's waits and commits
+//               overlap the other's issue window.
+//   warps 2-9   softmax + epilogue for head slot 0: warps 2-5 convert key
+//               columns 0..63 and write output features 0..63, warps 6-9
+//               columns 64..127 and features 64..127 (warp w reads TMEM lanes
+//               32 (w % 4) .. +31, so four consecutive warps cover rows 0..127)
+//   warps 10-17 the same for head slot 1
+// Four softmax warps per SMSP hide the latency of the special-function chain;
+// the two halves of a row add their partial row sums through shared memory.
 // TMEM (512 columns): per slot, S = Q K^T in 128 fp32 columns and O in 128.
 // The softmax warps overwrite S in place with P as two bf16 halves (hi, lo)
 // that sum to P to ~2^-16; O += P_hi V + P_lo V reads them straight from TMEM.
@@ -26,27 +38,30 @@
 // with no rescaling; the epilogue divides by the row sum once.
 //
 // Keys beyond the last visible row of an item's final tile may hold anything
-// (including NaN): the softmax gives them weight 0 by selection and the slot-0
+// (including NaN): the softmax gives them weight 0 by selection and the softmax
 // warps zero those rows of the staged V tile before the PV product reads it.
 #include "common.cuh"
 #include "host.cuh"
 
 namespace grok {
 
-constexpr int kPfThreads = 384;
+constexpr int kPfThreads = 608;
 constexpr int kPfRows = 128;   // query rows per tile (MMA M)
 constexpr int kPfKeys = 128;   // keys per K/V tile (MMA N for Q K^T, K for P V)
 constexpr int kPfStages = 2;
 constexpr int kBox = 128 * 128;             // [128 rows][64 bf16], 128-byte swizzled
 constexpr int kQBytes = 2 * 2 * kBox;       // two heads, two 64-wide halves of d
-constexpr int kKVBytes = 4 * kBox;          // K halves then V halves
-constexpr int kPfData = kQBytes + kPfStages * kKVBytes;
+constexpr int kTileBytes = 2 * kBox;        // one K or V tile: two 64-wide halves of d
+constexpr int kPfData = kQBytes + 2 * kPfStages * kTileBytes;
 
 struct PfBars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[kPfStages], kv_empty[kPfStages];
+  uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t mma_done;
+  uint64_t issue_turn[2];  // the issuers alternate: slot 0's tile-j MMAs, then slot 1's
+  uint64_t lsum_ready[2];  // both halves of a slot posted their partial row sums
+  float lsum[2][2][2][128];  // [item parity][slot][half][row]
   uint32_t tmem_base;
   int abort;
 };
@@ -92,29 +107,70 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
   return it;
 }
 
-__device__ __forceinline__ void pf_issue_qk(uint32_t tmem, int slot, uint32_t sq, uint32_t skv) {
+// MMA issue. The issuing thread shares its SMSP with busy softmax warps, so the
+// per-instruction work is kept to a descriptor add: the 64-bit descriptors of
+// the first K-step are built once and later steps add their byte offset / 16
+// to the start-address field (no carry: shared addresses are below 2^18).
+constexpr uint64_t kQSlotDesc = uint64_t((2 * kBox) >> 4);   // descriptor step between the slots' Q tiles
+constexpr uint64_t kStageDesc = uint64_t(kTileBytes >> 4);    // descriptor step between ring stages
+
+__device__ __forceinline__ void pf_issue_qk(uint32_t d, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kPfKeys, 0);
-  const uint32_t a0 = sq + slot * 2 * kBox;
-  const uint32_t d = tmem + slot * 256;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {  // K = 128 in steps of 16
-    const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-    umma_ss(d, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(skv + off, 16, 1024), idesc, kk > 0);
+    const uint64_t off = uint64_t(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+    umma_ss(d, qdesc + off, kdesc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void pf_issue_pv(uint32_t tmem, int slot, uint32_t skv, bool accumulate) {
+__device__ __forceinline__ void pf_issue_pv(uint32_t d, uint32_t pbase, uint64_t vdesc, bool accumulate) {
   constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kD, 1);  // V is N(d)-contiguous
-  const uint32_t v0 = skv + 2 * kBox;
-  const uint32_t d = tmem + slot * 256 + 128;
-  const uint32_t pbase = tmem + slot * 256;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
     // P for keys 32c..32c+31: hi in columns 32c..32c+15, lo in 32c+16..32c+31
     const uint32_t pcol = (kk >> 1) * 32 + (kk & 1) * 8;
-    const uint64_t bdesc = make_sdesc_sw128(v0 + kk * 2048, kBox, 1024);
-    umma_ts(d, pbase + pcol, bdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
-    umma_ts(d, pbase + pcol + 16, bdesc, idesc, 1u);
+    const uint64_t b = vdesc + uint64_t((kk * 2048) >> 4);
+    umma_ts(d, pbase + pcol, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(d, pbase + pcol + 16, b, idesc, 1u);
+  }
+}
+
+// S -> P for one 128-key tile of one row (this thread's TMEM lane): weights
+// exp(c - 30), zero where masked, accumulated into the row sum and written back
+// over S as bf16 hi/lo halves (keys 32c..32c+31: hi in columns 32c..32c+15, lo
+// in 32c+16..32c+31). TMEM loads are double-buffered: the next 32 columns are
+// in flight while the current ones are converted.
+template <bool kMask>
+__device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c, int rel, float& l0, float& l1,
+                                                 uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float w0 = capped_weight(__uint_as_float(sv[2 * e]));
+    float w1 = capped_weight(__uint_as_float(sv[2 * e + 1]));
+    if (kMask) {
+      w0 = (c * 32 + 2 * e <= rel) ? w0 : 0.f;
+      w1 = (c * 32 + 2 * e + 1 <= rel) ? w1 : 0.f;
+    }
+    l0 += w0;
+    l1 += w1;
+    split_bf16x2(w0, w1, hi[e], lo[e]);
+  }
+}
+
+// One warp's half of a tile: key columns 64 half .. 64 half + 63 of its rows,
+// in two 32-column chunks (a TMEM load returns in ~30 cycles, so no prefetch).
+template <bool kMask>
+__device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel, float& l0, float& l1) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * half + cc;
+    uint32_t a[32];
+    uint32_t hi[16], lo[16];
+    tmem_ld32(trow + c * 32, a);
+    tmem_wait_ld_dep(a);
+    pf_softmax_chunk<kMask>(a, c, rel, l0, l1, hi, lo);
+    tmem_st16(trow + c * 32, hi);
+    tmem_st16(trow + c * 32 + 16, lo);
   }
 }
 
@@ -124,25 +180,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = smem + kQBytes;
+  uint8_t* sK = smem + kQBytes;                           // K ring
+  uint8_t* sV = sK + kPfStages * kTileBytes;              // V ring
   PfBars* bars = reinterpret_cast<PfBars*>(smem + kPfData);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, 2);
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 2);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->p_full[s], 256);
       mbar_init(&bars->o_full[s], 1);
-      mbar_init(&bars->o_empty[s], 128);
+      mbar_init(&bars->o_empty[s], 256);
+      mbar_init(&bars->lsum_ready[s], 256);
     }
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done, 2);
+    mbar_init(&bars->issue_turn[0], 1);
+    mbar_init(&bars->issue_turn[1], 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -178,76 +240,89 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         bool ok = true;
         for (int j = 0; j < it.n_kv; ++j, ++kv_it) {
           const int st = kv_it % kPfStages;
-          if (!mbar_wait(&bars->kv_empty[st], ((kv_it / kPfStages) & 1) ^ 1, abort, p.status)) {
+          const uint32_t par = ((kv_it / kPfStages) & 1) ^ 1;
+          if (!mbar_wait(&bars->k_empty[st], par, abort, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->kv_full[st], kKVBytes);
-          uint8_t* base = sKV + st * kKVBytes;
-          tma_load_4d(base, &tm_k, &bars->kv_full[st], 0, it.g, j * kPfKeys, it.b);
-          tma_load_4d(base + kBox, &tm_k, &bars->kv_full[st], 64, it.g, j * kPfKeys, it.b);
-          tma_load_4d(base + 2 * kBox, &tm_v, &bars->kv_full[st], 0, it.g, j * kPfKeys, it.b);
-          tma_load_4d(base + 3 * kBox, &tm_v, &bars->kv_full[st], 64, it.g, j * kPfKeys, it.b);
+          mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
+          tma_load_4d(sK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, it.g, j * kPfKeys, it.b);
+          tma_load_4d(sK + st * kTileBytes + kBox, &tm_k, &bars->k_full[st], 64, it.g, j * kPfKeys, it.b);
+          if (!mbar_wait(&bars->v_empty[st], par, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
+          tma_load_4d(sV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, it.g, j * kPfKeys, it.b);
+          tma_load_4d(sV + st * kTileBytes + kBox, &tm_v, &bars->v_full[st], 64, it.g, j * kPfKeys, it.b);
         }
         if (!ok) break;
       }
       // Drain: copies still in flight (only after an abort) land before the CTA exits.
       volatile int never = 0;
-      for (int t = max(0, kv_it - kPfStages); t < kv_it; ++t)
-        mbar_wait(&bars->kv_full[t % kPfStages], (t / kPfStages) & 1, &never, p.status);
+      for (int t = max(0, kv_it - kPfStages); t < kv_it; ++t) {
+        mbar_wait(&bars->k_full[t % kPfStages], (t / kPfStages) & 1, &never, p.status);
+        mbar_wait(&bars->v_full[t % kPfStages], (t / kPfStages) & 1, &never, p.status);
+      }
       if (q_it > 0) mbar_wait(&bars->q_full, (q_it - 1) & 1, &never, p.status);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 18) {
+    // ------------------------------------------------------------ MMA issuers (one per slot)
     if (lane == 0) {
-      const uint32_t sq = smem_u32(sQ), skv0 = smem_u32(sKV);
+      const int slot = warp == 1 ? 0 : 1;
+      const uint32_t s_tm = tmem + slot * 256, o_tm = s_tm + 128;
+      const uint64_t qd = make_sdesc_sw128(smem_u32(sQ), 16, 1024) + slot * kQSlotDesc;
+      const uint64_t kd = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vd = make_sdesc_sw128(smem_u32(sV), kBox, 1024);
       int kv_it = 0, q_it = 0, item_it = 0;
+      int turns = 0;  // turns taken by this issuer; slot 0 starts
       bool ok = true;
+      auto take_turn = [&]() -> bool {
+        const uint32_t par = uint32_t(turns & 1) ^ (slot == 0 ? 1u : 0u);
+        return mbar_wait(&bars->issue_turn[slot], par, abort, p.status);
+      };
+      auto pass_turn = [&]() {
+        mbar_arrive(&bars->issue_turn[slot ^ 1]);
+        ++turns;
+      };
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         const PfItem it = pf_item(p, item);
         if (it.n_kv == 0) continue;
         if (!mbar_wait(&bars->q_full, q_it & 1, abort, p.status)) break;
         {
           const int st = kv_it % kPfStages;
-          if (!mbar_wait(&bars->kv_full[st], (kv_it / kPfStages) & 1, abort, p.status)) break;
+          if (!mbar_wait(&bars->k_full[st], (kv_it / kPfStages) & 1, abort, p.status) || !take_turn()) break;
           tc_fence_after();
-          for (int slot = 0; slot < 2; ++slot) {
-            pf_issue_qk(tmem, slot, sq, skv0 + st * kKVBytes);
-            umma_commit(&bars->s_full[slot]);
-          }
+          pf_issue_qk(s_tm, qd, kd + st * kStageDesc);
+          pass_turn();
+          umma_commit(&bars->s_full[slot]);
+          umma_commit(&bars->k_empty[st]);
         }
-        for (int j = 0; j < it.n_kv && ok; ++j) {
+        for (int j = 0; j < it.n_kv; ++j) {
           const int cur = kv_it + j;
           const int st = cur % kPfStages;
           const bool has_next = j + 1 < it.n_kv;
           const int stn = (cur + 1) % kPfStages;
+          if (!mbar_wait(&bars->v_full[st], (cur / kPfStages) & 1, abort, p.status) ||
+              (has_next && !mbar_wait(&bars->k_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status)) ||
+              !mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status) ||
+              (j == 0 && !mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status)) ||
+              !take_turn()) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          pf_issue_pv(o_tm, s_tm, vd + st * kStageDesc, j > 0);
+          if (has_next) pf_issue_qk(s_tm, qd, kd + stn * kStageDesc);
+          pass_turn();
+          umma_commit(&bars->v_empty[st]);
           if (has_next) {
-            if (!mbar_wait(&bars->kv_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status)) {
-              ok = false;
-              break;
-            }
+            umma_commit(&bars->s_full[slot]);
+            umma_commit(&bars->k_empty[stn]);
+          } else {
+            umma_commit(&bars->o_full[slot]);
+            umma_commit(&bars->q_empty);
           }
-          for (int slot = 0; slot < 2; ++slot) {
-            if (!mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status)) {
-              ok = false;
-              break;
-            }
-            if (j == 0 && !mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            pf_issue_pv(tmem, slot, skv0 + st * kKVBytes, j > 0);
-            if (has_next) {
-              pf_issue_qk(tmem, slot, sq, skv0 + stn * kKVBytes);
-              umma_commit(&bars->s_full[slot]);
-            } else {
-              umma_commit(&bars->o_full[slot]);
-            }
-          }
-          if (!ok) break;
-          umma_commit(&bars->kv_empty[st]);
-          if (!has_next) umma_commit(&bars->q_empty);
         }
         kv_it += it.n_kv;
         ++q_it;
@@ -258,9 +333,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       volatile int never = 0;
       mbar_wait(&bars->mma_done, 0, &never, p.status);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2 && warp <= 17) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int slot = (warp - 4) >> 2;
+    const int slot = (warp - 2) >> 3;
+    const int half = ((warp - 2) >> 2) & 1;    // key columns / output features 64 half ..
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // query row within the tile
     const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
@@ -268,7 +344,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
       const PfItem it = pf_item(p, item);
       if (it.n_kv == 0) {
-        if (it.bad && slot == 0 && r == 0) report(p.status, it.bad);
+        if (it.bad && slot == 0 && half == 0 && r == 0) report(p.status, it.bad);
         continue;
       }
       const int i = it.qt * kPfRows + r;
@@ -276,38 +352,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       float l0 = 0.f, l1 = 0.f;
       bool ok = true;
       for (int j = 0; j < it.n_kv; ++j) {
-        if (!mbar_wait(&bars->s_full[slot], (tile_cnt + j) & 1, abort, p.status)) {
+        ok = mbar_wait(&bars->s_full[slot], (tile_cnt + j) & 1, abort, p.status);
+        if (!__all_sync(0xffffffffu, ok)) {  // leave together: the TMEM ops below are warp-collective
           ok = false;
           break;
         }
         tc_fence_after();
         const int rel = lim - j * kPfKeys;       // columns c <= rel are visible
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {            // 32 keys at a time
-          uint32_t sv[32];
-          tmem_ld32(trow + c * 32, sv);
-          tmem_wait_ld();
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float w0 = capped_weight(__uint_as_float(sv[2 * e]));
-            float w1 = capped_weight(__uint_as_float(sv[2 * e + 1]));
-            w0 = (c * 32 + 2 * e <= rel) ? w0 : 0.f;
-            w1 = (c * 32 + 2 * e + 1 <= rel) ? w1 : 0.f;
-            l0 += w0;
-            l1 += w1;
-            split_bf16x2(w0, w1, hi[e], lo[e]);
-          }
-          tmem_st16(trow + c * 32, hi);
-          tmem_st16(trow + c * 32 + 16, lo);
-        }
-        if (slot == 0 && j == it.n_kv - 1) {
+        // The choice must be warp-uniform: the TMEM loads and stores inside
+        // are warp-collective (.sync.aligned).
+        if (__all_sync(0xffffffffu, rel >= kPfKeys - 1))
+          pf_softmax_half<false>(trow, half, rel, l0, l1);
+        else
+          pf_softmax_half<true>(trow, half, rel, l0, l1);
+        if (half == 0 && j == it.n_kv - 1) {
           // Zero the V rows of the last tile that lie beyond every visible key.
+          // Both slots do it (same zeros) before handing over their P, since
+          // each slot's PV product may be issued first.
           const int first_dead = it.kv_end - j * kPfKeys;
           if (r >= first_dead) {
             const int st = (tile_cnt + j) % kPfStages;
-            uint4* v0 = reinterpret_cast<uint4*>(sKV + st * kKVBytes + 2 * kBox + r * 128);
-            uint4* v1 = reinterpret_cast<uint4*>(sKV + st * kKVBytes + 3 * kBox + r * 128);
+            uint4* v0 = reinterpret_cast<uint4*>(sV + st * kTileBytes + r * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(sV + st * kTileBytes + kBox + r * 128);
             const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -323,24 +389,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (!ok) break;
       tile_cnt += it.n_kv;
-      // epilogue: O / l -> bf16
-      if (!mbar_wait(&bars->o_full[slot], item_it & 1, abort, p.status)) break;
+      // row sum of both halves (double-buffered by item parity)
+      bars->lsum[item_it & 1][slot][half][r] = l0 + l1;
+      mbar_arrive(&bars->lsum_ready[slot]);
+      // epilogue: O / l -> bf16 for this half's 64 output features
+      ok = mbar_wait(&bars->lsum_ready[slot], item_it & 1, abort, p.status) &&
+           mbar_wait(&bars->o_full[slot], item_it & 1, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const float inv_l = 1.0f / (l0 + l1);
+      const float inv_l = 1.0f / (bars->lsum[item_it & 1][slot][0][r] + bars->lsum[item_it & 1][slot][1][r]);
       const int h = it.g * kGroup + it.hp * 2 + slot;
-      uint4* dst = p.out + (((size_t)it.b * p.T + i) * kQHeads + h) * 16;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      uint4* dst = p.out + (((size_t)it.b * p.T + i) * kQHeads + h) * 16 + half * 8;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t ov[32];
-        tmem_ld32(trow + 128 + c * 32, ov);
-        tmem_wait_ld();
+        tmem_ld32(trow + 128 + half * 64 + cc * 32, ov);
+        tmem_wait_ld_dep(ov);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
         if (i < p.T) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[c * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            dst[cc * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
       tc_fence_before();

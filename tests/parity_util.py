@@ -10,6 +10,9 @@ must match bit for bit.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from oracle import bf16
@@ -37,6 +40,10 @@ def compare(got_bits: np.ndarray, ref_bits: np.ndarray) -> dict:
 
 def assert_close(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "") -> dict:
     st = compare(got_bits, ref_bits)
+    log = os.environ.get("GROK_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, "n": int(got_bits.size), **st}) + "\n")
     assert st["finite"], f"{what}: non-finite outputs"
     assert st["mean_abs"] <= MEAN_TOL, f"{what}: mean abs {st['mean_abs']:.3e} > {MEAN_TOL} ({st})"
     assert st["max_ulps_above_tol"] <= 1, f"{what}: elements above {MAX_TOL} beyond one bf16 ulp ({st})"

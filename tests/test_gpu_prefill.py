@@ -90,7 +90,7 @@ def test_prefill_one_visible_key_copies_v():
     inp = W.custom(B=1, T=64, Tmax=64, start_pos=[0], valid_len=[1], seed=24)
     oq, ok_, ov, out, status = run_prefill(inp)
     assert status == 0
-    want = np.repeat(ov[0, 0][None], 6, axis=0).reshape(48, 128)     # head h reads kv head h // 6
+    want = np.repeat(ov[0, 0], 6, axis=0)     # [48, 128]: head h reads kv head h // 6
     for i in range(64):
         assert np.array_equal(out[0, i], want)
 
