@@ -35,6 +35,7 @@ EXPORTS = (
     "grok_attn_decode_workspace",
     "grok_attn_decode",
     "grok_attn_combine",
+    "grok_attn_decode_step_static",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -69,6 +70,8 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_decode.argtypes = [P, P, P, P, I, I, P, S, P, P]
     lib.grok_attn_combine.restype = I
     lib.grok_attn_combine.argtypes = [P, S, P, I, I, P, P, P]
+    lib.grok_attn_decode_step_static.restype = I
+    lib.grok_attn_decode_step_static.argtypes = [P, P, P, P, I, I, P, P, P]
     _lib = lib
     return lib
 
@@ -179,6 +182,24 @@ def combine(workspace, kv_len, out, Tmax: int, dev_status=None, stream=None) -> 
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().grok_attn_combine(_ptr(workspace), nbytes, _ptr(kv_len), B, Tmax, _ptr(out),
                                     _ptr(dev_status), _stream(stream)))
+
+
+def decode_step_static(q_rot, cache_k, cache_v, kv_len, out, dev_status=None, stream=None) -> None:
+    """A decode step that allocates nothing: the library's static workspace holds the partial sums.
+
+    For callers that cannot allocate device memory. Calls that overlap on the
+    GPU share that workspace and race; see grok_attn_decode_step_static.
+    """
+    B, Tmax = cache_k.shape[0], cache_k.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(kv_len, "kv_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_attn_decode_step_static(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(kv_len), B, Tmax,
+                                               _ptr(out), _ptr(dev_status), _stream(stream)))
 
 
 def decode_step(q_rot, cache_k, cache_v, kv_len, workspace, out, dev_status=None, stream=None) -> None:

@@ -15,6 +15,8 @@
 // logit is below 30), and O += P_hi V + P_lo V with P split into two bf16
 // halves. Each split writes its unnormalised O and row sum l; the combine
 // kernel adds the splits and divides.
+#include <mutex>
+
 #include "common.cuh"
 #include "host.cuh"
 
@@ -325,4 +327,66 @@ extern "C" grok_status grok_attn_combine(const void* workspace, size_t workspace
   combine_kernel<<<dim3(kKVHeads, B), 192, 0, static_cast<cudaStream_t>(stream)>>>(
       dec_ws(const_cast<void*>(workspace), B, ns), kv_len, Tmax, ns, reinterpret_cast<uint2*>(out), dev_status);
   return check_launch("combine");
+}
+
+// ----------------------------------------------------------------------------
+// Decode step with library-owned scratch, for callers that may not allocate.
+//
+// Some callers cannot hand this library a workspace: a host framework that
+// owns every byte of device memory and gives its plugins no allocator, or a
+// serving loop whose memory plan is fixed up front and where cudaMalloc, which
+// may synchronise the device and take milliseconds, is not allowed between
+// steps. For them the split-K partial sums live in this file-scope array. It
+// is allocated when the library is loaded, on every GPU that loads it, and
+// held until the process exits.
+static __device__ __align__(256) unsigned char g_static_ws[GROK_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+// Device address of g_static_ws on each device. In host code the symbol itself
+// is only a host-side stand-in, so the address must come from the runtime.
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {nullptr};
+
+grok_status static_ws_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(GROK_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess || !p)
+      return fail(GROK_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return GROK_OK;
+}
+
+}  // namespace
+
+extern "C" grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16* cache_k,
+                                                    const grok_bf16* cache_v, const int32_t* kv_len, int B,
+                                                    int Tmax, grok_bf16* out, int32_t* dev_status,
+                                                    void* stream) {
+  if (B < 1 || Tmax < 1 || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step_static: need B >= 1, 1 <= Tmax <= %d",
+                GROK_MAX_POSITION);
+  const int ns = (Tmax + kDecSplit - 1) / kDecSplit;
+  const size_t need = dec_ws_bytes(B, ns);
+  if (need > sizeof(g_static_ws))
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_attn_decode_step_static: B=%d, Tmax=%d needs %zu bytes of scratch, more than the %zu "
+                "bytes of the library's static workspace (use grok_attn_decode with a caller workspace)",
+                B, Tmax, need, sizeof(g_static_ws));
+  void* ws = nullptr;
+  grok_status st = static_ws_address(&ws);
+  if (st != GROK_OK) return st;
+  // Every partial sum the combine reads is written by the decode launch just
+  // before it, so the scratch needs no clearing between calls.
+  if ((st = grok_attn_decode(q_rot, cache_k, cache_v, kv_len, B, Tmax, ws, need, dev_status, stream)) != GROK_OK)
+    return st;
+  return grok_attn_combine(ws, need, kv_len, B, Tmax, out, dev_status, stream);
 }

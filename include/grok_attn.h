@@ -145,6 +145,34 @@ grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k, c
 grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len, int B,
                               int Tmax, grok_bf16* out, int32_t* dev_status, void* stream);
 
+/* Size of the library's static decode workspace (bytes). */
+#define GROK_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * A whole decode step (grok_attn_decode then grok_attn_combine) that
+ * allocates nothing and takes no workspace. The pages have no counterpart:
+ * this call exists for callers that cannot allocate device memory, such as a
+ * plugin whose host framework owns all device memory, or a serving loop whose
+ * memory is planned up front and may not call cudaMalloc (which can
+ * synchronise the device) between steps.
+ *
+ * The split-K partial sums go to a static device array of
+ * GROK_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * the process exits; shapes whose workspace (grok_attn_decode_workspace) is
+ * larger are rejected with GROK_ERR_INVALID_ARG. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current, so make the first call on each device before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (different
+ * streams, or different host threads on the same device) race and give wrong
+ * results; calls ordered on one stream are safe. Nothing needs clearing: each
+ * call writes every partial sum it reads. Arguments and results are those of
+ * grok_attn_decode + grok_attn_combine:
+ *   q_rot [B,48,128]; cache_k, cache_v [B,Tmax,8,128]; kv_len [B] int32; out [B,48,128].
+ */
+grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
+                                         const int32_t* kv_len, int B, int Tmax, grok_bf16* out,
+                                         int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
