@@ -74,6 +74,33 @@ def append_bytes(B: int, T: int) -> float:
     return 2.0 * B * T * 64 * 128 * 2
 
 
+def source_digest(*paths: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+KERNEL_SOURCES = {
+    "prefill_kernel": ("grok_gqa_attention_gb300/csrc/prefill.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
+    "decode_kernel": ("grok_gqa_attention_gb300/csrc/decode.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
+}
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu capture, or None if the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("source_sha256") != source_digest(*KERNEL_SOURCES[kernel]):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -297,7 +324,7 @@ def run_ours(args, rank: int, world: int, dist):
         "kernels_ms": {"rope_kv_append": ms_append, "prefill": ms_prefill},
         "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": prefill_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": prefill_tflops / peak_tf, "peak_source": f"bf16_tflops ({peak_kind})",
-                     "traffic": None},
+                     "traffic": measured_traffic("prefill_kernel"), "traffic_unit": "bytes per launch (ncu)"},
         "append": {"GB/s": append_bytes(B, T) / (ms_append * 1e-3) / 1e9,
                    "frac_of_hbm": append_bytes(B, T) / (ms_append * 1e-3) / 1e9 / peak_bw},
         "clocks": clk,
@@ -415,7 +442,7 @@ def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
         "l2": f"{n_copies} rotating cache copies of {nbytes / 1e6:.0f} MB used rows each",
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs_kernel, "peak": peak_bw,
                      "unit": "GB/s", "frac": gbs_kernel / peak_bw, "peak_source": f"hbm_gbs ({peak_kind})",
-                     "traffic": None},
+                     "traffic": measured_traffic("decode_kernel"), "traffic_unit": "bytes per launch (ncu)"},
         "gpu_launches": 3 * args.steps,
     }
 
