@@ -110,6 +110,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Elementwise maximum of per-rank timings (identity on one rank)."""
+    values = [float(x) for x in values]
+    if dist is None:
+        return values
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(work_per_rank: float, world: int, ms_max: float, scale: float) -> float:
+    """Weak scaling: every rank processes work_per_rank units; the job ends with the slowest rank."""
+    return world * work_per_rank / (ms_max * 1e-3) / scale
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -296,11 +313,8 @@ def run_ours(args, rank: int, world: int, dist):
     ms = t_start.elapsed_time(t_end) / args.steps
     ms_append = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     ms_prefill = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    if dist:
-        t = torch.tensor([ms, ms_prefill, ms_append], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_prefill, ms_append = (float(x) for x in t.tolist())
-    value = world * flops / (ms * 1e-3) / 1e12
+    ms, ms_prefill, ms_append = max_over_ranks([ms, ms_prefill, ms_append], dist, dev)
+    value = whole_job_rate(flops, world, ms, 1e12)
     prefill_tflops = flops / (ms_prefill * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -358,12 +372,9 @@ def run_ours(args, rank: int, world: int, dist):
         b_.record(stream)
         torch.cuda.synchronize()
         ms_e2e = a.elapsed_time(b_) / args.steps
-        if dist:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        (ms_e2e,) = max_over_ranks([ms_e2e], dist, dev)
         h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh, sh))
-        result["e2e"] = {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        result["e2e"] = {"value": whole_job_rate(flops, world, ms_e2e, 1e12), "unit": "TFLOP/s",
                          "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": oh.numel() * oh.element_size()}
         del qh, kh, vh, oh
@@ -428,12 +439,9 @@ def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
     ms_dec = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     ms_comb = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
     ms_app = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    if dist:
-        t = torch.tensor([ms, ms_dec], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_dec = (float(x) for x in t.tolist())
+    ms, ms_dec = max_over_ranks([ms, ms_dec], dist, dev)
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    gbs_step = world * nbytes / (ms * 1e-3) / 1e9
+    gbs_step = whole_job_rate(nbytes, world, ms, 1e9)
     gbs_kernel = nbytes / (ms_dec * 1e-3) / 1e9
     return {
         "workload": DECODE_WORKLOAD, "value": gbs_step, "unit": "GB/s", "ms_per_step": ms,

@@ -36,6 +36,7 @@ EXPORTS = (
     "grok_attn_decode",
     "grok_attn_combine",
     "grok_attn_decode_step_static",
+    "grok_selftest_bounded_wait",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -70,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_decode.argtypes = [P, P, P, P, I, I, P, S, P, P]
     lib.grok_attn_combine.restype = I
     lib.grok_attn_combine.argtypes = [P, S, P, I, I, P, P, P]
+    lib.grok_selftest_bounded_wait.restype = I
+    lib.grok_selftest_bounded_wait.argtypes = [P, P, ctypes.c_longlong, P]
     lib.grok_attn_decode_step_static.restype = I
     lib.grok_attn_decode_step_static.argtypes = [P, P, P, P, I, I, P, P, P]
     _lib = lib
@@ -182,6 +185,13 @@ def combine(workspace, kv_len, out, Tmax: int, dev_status=None, stream=None) -> 
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().grok_attn_combine(_ptr(workspace), nbytes, _ptr(kv_len), B, Tmax, _ptr(out),
                                     _ptr(dev_status), _stream(stream)))
+
+
+def selftest_bounded_wait(dev_status, flags, limit_cycles: int, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (see grok_selftest_bounded_wait)."""
+    _want(dev_status, "dev_status", torch.int32, (1,))
+    _want(flags, "flags", torch.int32, (2,))
+    _check(load().grok_selftest_bounded_wait(_ptr(dev_status), _ptr(flags), int(limit_cycles), _stream(stream)))
 
 
 def decode_step_static(q_rot, cache_k, cache_v, kv_len, out, dev_status=None, stream=None) -> None:

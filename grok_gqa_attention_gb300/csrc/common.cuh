@@ -82,21 +82,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity. Returns false (after
-// recording a timeout and raising *abort) if the wait gives up, or immediately
-// if another thread of the CTA already raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int32_t* status) {
+// recording a timeout and raising *abort) if the wait gives up after
+// `limit` clock cycles, or as soon as another thread of the CTA has raised
+// *abort.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > GROK_WAIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       report(status, GROK_DEV_TIMEOUT);
       *abort = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int32_t* status) {
+  return mbar_wait_for(bar, parity, abort, status, GROK_WAIT_CYCLES);
 }
 
 // ----------------------------------------------------------------------------

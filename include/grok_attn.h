@@ -145,6 +145,18 @@ grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k, c
 grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len, int B,
                               int Tmax, grok_bf16* out, int32_t* dev_status, void* stream);
 
+/*
+ * Failure-detection self-test. Every wait inside the pipelined kernels is
+ * bounded: after a clock-cycle limit it ORs GROK_DEV_TIMEOUT into *dev_status,
+ * raises its CTA's abort flag so the other waiting warps leave too, and the
+ * kernel returns without trapping. This call runs that machinery on a
+ * one-CTA kernel whose two barriers nothing ever completes: warp 0 waits
+ * limit_cycles and gives up, warp 1 (limit 1000x longer) must leave through
+ * the abort flag. Afterwards *dev_status has GROK_DEV_TIMEOUT and
+ * flags[0] = flags[1] = 2 (device int32[2]). limit_cycles in [1, 4e9].
+ */
+grok_status grok_selftest_bounded_wait(int32_t* dev_status, int32_t* flags, long long limit_cycles, void* stream);
+
 /* Size of the library's static decode workspace (bytes). */
 #define GROK_STATIC_WORKSPACE_BYTES (16u << 20)
 
