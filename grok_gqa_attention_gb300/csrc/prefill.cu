@@ -303,11 +303,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int st = cur % kPfStages;
           const bool has_next = j + 1 < it.n_kv;
           const int stn = (cur + 1) % kPfStages;
+          // Every wait that is normally already satisfied comes first; the wait
+          // for this slot's P, the real dependency, comes last so that only it
+          // (about 100 cycles even when ready) sits between P and the products.
           if (!mbar_wait(&bars->v_full[st], (cur / kPfStages) & 1, abort, p.status) ||
               (has_next && !mbar_wait(&bars->k_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status)) ||
-              !mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status) ||
               (j == 0 && !mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status)) ||
-              !take_turn()) {
+              !take_turn() || !mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status)) {
             ok = false;
             break;
           }
