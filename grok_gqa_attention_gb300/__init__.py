@@ -31,6 +31,7 @@ EXPORTS = (
     "grok_abi_version",
     "grok_last_error",
     "grok_rope_kv_append",
+    "grok_rope_cos_sin",
     "grok_attn_prefill",
     "grok_attn_decode_workspace",
     "grok_attn_decode",
@@ -63,6 +64,8 @@ def load() -> ctypes.CDLL:
     lib.grok_last_error.argtypes = []
     lib.grok_rope_kv_append.restype = I
     lib.grok_rope_kv_append.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P]
+    lib.grok_rope_cos_sin.restype = I
+    lib.grok_rope_cos_sin.argtypes = [I, I, P, P, P]
     lib.grok_attn_prefill.restype = I
     lib.grok_attn_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
     lib.grok_attn_decode_workspace.restype = I
@@ -126,6 +129,14 @@ def rope_kv_append(q, k, v, start_pos, q_rot, cache_k, cache_v, dev_status=None,
         _want(dev_status, "dev_status", torch.int32, (1,))
     _check(load().grok_rope_kv_append(_ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), B, T, Tmax, _ptr(q_rot),
                                       _ptr(cache_k), _ptr(cache_v), _ptr(dev_status), _stream(stream)))
+
+
+def rope_cos_sin(first_position: int, n_positions: int, stream=None):
+    """The fp32 cos/sin table [n_positions, 64] the append kernel uses (new CUDA tensors)."""
+    c = torch.empty((n_positions, 64), dtype=torch.float32, device="cuda")
+    s = torch.empty_like(c)
+    _check(load().grok_rope_cos_sin(int(first_position), int(n_positions), _ptr(c), _ptr(s), _stream(stream)))
+    return c, s
 
 
 def prefill(q_rot, cache_k, cache_v, start_pos, valid_len, out, dev_status=None, stream=None) -> None:

@@ -6,11 +6,11 @@
 // rotated with offset = step before the cache write; V written unrotated;
 // update_into at step[b]).
 //
-// One CTA iteration handles one token (b, i): 64 threads evaluate the 64
-// (cos, sin) pairs of its position in fp64 and round them to fp32; then the
-// CTA streams the token's 48 query heads and 8 key heads (128-bit loads of 8
-// bf16 of the first half and the matching 8 of the second half) and its 8
-// value heads. The rotation uses separately rounded fp32 multiplies and adds
+// One warp handles one token (b, i): its lanes evaluate the 64 (cos, sin)
+// pairs of the token's position in fp64 and round them to fp32; then the warp
+// streams the token's 48 query heads and 8 key heads (128-bit loads of 8 bf16
+// of the first half and the matching 8 of the second half) and its 8 value
+// heads. The rotation uses separately rounded fp32 multiplies and adds
 // (no FMA contraction), so the result is bit-for-bit the fp32 chain.
 //
 // Memory-bound: per token it reads 14 KB (q, k, v) and writes 14 KB.
@@ -20,8 +20,64 @@
 namespace grok {
 
 constexpr int kRopeThreads = 128;
-constexpr int kRopeUnits = (kQHeads + kKVHeads) * 8;  // 8 groups of 8 pairs per head
-constexpr int kVUnits = kKVHeads * kD / 8;             // uint4 units of V per token
+
+// cos and sin of an fp32 phase (0 <= phase < 65536), evaluated in fp64 and
+// rounded once to fp32. Reduction by pi/2 (Cody-Waite): pi/2 is split into
+// three doubles, the first two with 33 significant bits so that k * C1 and
+// k * C2 are exact for k < 2^20, the third the remaining bits (pi/2 - C1 - C2 -
+// C3 ~ 1e-37); each fused step rounds relative to its own result, so the
+// reduced argument r (|r| <= pi/4, never below 2.7e-7 for a nonzero phase in
+// this domain) carries about two ulps of relative error. sin and cos of r are
+// Taylor polynomials through r^15 and r^14 (truncation below 2^-50 on
+// |r| <= pi/4). The result is well inside the margin the fp32 rounding needs:
+// for these phases every exact value lies at least 59 fp64 ulps from an fp32
+// rounding midpoint, so the rounded table is the correctly rounded one.
+__device__ __forceinline__ void rope_cos_sin(float phase, float& c_out, float& s_out) {
+  constexpr double kTwoOverPi = 0x1.45f306dc9c883p-1;
+  constexpr double C1 = 0x1.921fb54400000p+0;
+  constexpr double C2 = 0x1.0b4611a600000p-34;
+  constexpr double C3 = 0x1.3198a2e037073p-69;
+  const double x = double(phase);
+  const double k = rint(x * kTwoOverPi);
+  double r = fma(-k, C1, x);
+  r = fma(-k, C2, r);
+  r = fma(-k, C3, r);
+  const double r2 = r * r;
+  // sin r = r + r^3 (-1/3! + r^2 (1/5! - ... + r^2 (-1/15!)))
+  double sp = -1.0 / 1307674368000.0;
+  sp = fma(sp, r2, 1.0 / 6227020800.0);
+  sp = fma(sp, r2, -1.0 / 39916800.0);
+  sp = fma(sp, r2, 1.0 / 362880.0);
+  sp = fma(sp, r2, -1.0 / 5040.0);
+  sp = fma(sp, r2, 1.0 / 120.0);
+  sp = fma(sp, r2, -1.0 / 6.0);
+  const double sr = fma(r * r2, sp, r);
+  // cos r = 1 + r^2 (-1/2! + r^2 (1/4! - ... + r^2 (1/14!)))
+  double cp = -1.0 / 87178291200.0;
+  cp = fma(cp, r2, 1.0 / 479001600.0);
+  cp = fma(cp, r2, -1.0 / 3628800.0);
+  cp = fma(cp, r2, 1.0 / 40320.0);
+  cp = fma(cp, r2, -1.0 / 720.0);
+  cp = fma(cp, r2, 1.0 / 24.0);
+  cp = fma(cp, r2, -0.5);
+  const double cr = fma(r2, cp, 1.0);
+  // phase = k pi/2 + r
+  const int q = int(k) & 3;
+  const double sv = (q == 0) ? sr : (q == 1) ? cr : (q == 2) ? -sr : -cr;
+  const double cv = (q == 0) ? cr : (q == 1) ? -sr : (q == 2) ? -cr : sr;
+  c_out = __double2float_rn(cv);
+  s_out = __double2float_rn(sv);
+}
+
+// inv_freq[j] = 1 / RN32(10000^(2j/128)): the power in fp64 rounded once to
+// fp32, then an fp32 division. 10000^(j/64) = 2^(j log2(10000) / 64); with
+// log2(10000) rounded to double and exp2 within an ulp the power carries a
+// few fp64 ulps of error, far inside the margin its fp32 rounding needs (every
+// 10000^(j/64), j < 64, lies more than 4e6 fp64 ulps from an fp32 midpoint).
+__device__ __forceinline__ float rope_inv_freq(int j) {
+  constexpr double kLog2Base = 13.287712379549449;  // log2(10000)
+  return __fdiv_rn(1.0f, __double2float_rn(exp2(double(j) * (kLog2Base / 64.0))));
+}
 
 __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const float* c, const float* s,
                                         uint4& y1, uint4& y2) {
@@ -45,65 +101,90 @@ __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const 
   y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
 }
 
+// A team of `team` warps (1, 2, 4 or 8) per token, grid-stride over tokens
+// with no CTA-wide barrier: every warp of the team evaluates the token's 64
+// (cos, sin) pairs into its own shared-memory slice, then warp w of the team
+// takes the rotation units (8 pairs of one head) and value units whose index m
+// satisfies m % team == w, unrolled so that its loads are in flight together.
+// Large batches use one warp per token; a handful of tokens (a decode step)
+// spreads each token over eight warps.
+constexpr int kRopeWarps = kRopeThreads / 32;
+
+template <int team>
 __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int32_t* __restrict__ start_pos, int B, int T, int Tmax, uint4* __restrict__ q_rot,
     uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, int32_t* status) {
   __shared__ float s_inv[64];
-  __shared__ float s_cos[64];
-  __shared__ float s_sin[64];
-  const int tid = threadIdx.x;
-  if (tid < 64) {
-    // inv_freq[j] = 1 / RN32(10000^(2j/128)): fp64 power rounded once, fp32 division
-    const float p32 = __double2float_rn(pow(10000.0, double(tid) / 64.0));
-    s_inv[tid] = __fdiv_rn(1.0f, p32);
-  }
+  __shared__ float s_cos[kRopeWarps][64];
+  __shared__ float s_sin[kRopeWarps][64];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < 64) s_inv[tid] = rope_inv_freq(tid);
+  __syncthreads();
   const long long ntok = (long long)B * T;
-  for (long long tok = blockIdx.x; tok < ntok; tok += gridDim.x) {
+  const long long gw = (long long)blockIdx.x * kRopeWarps + warp;
+  const int member = int(gw % team);
+  const long long n_teams = (long long)gridDim.x * kRopeWarps / team;
+  for (long long tok = gw / team; tok < ntok; tok += n_teams) {
     const int b = int(tok / T);
     const int i = int(tok - (long long)b * T);
-    const int s0 = start_pos[b];
+    const int s0 = __ldg(start_pos + b);
     const bool ok = s0 >= 0 && (long long)s0 + T <= Tmax && (long long)s0 + T <= GROK_MAX_POSITION;
-    if (!ok) {  // uniform over the CTA
-      if (tid == 0 && i == 0) report(status, GROK_DEV_BAD_START);
+    if (!ok) {  // uniform over the warp
+      if (lane == 0 && i == 0 && member == 0) report(status, GROK_DEV_BAD_START);
       continue;
     }
     const int pos = s0 + i;
-    __syncthreads();  // previous token's table no longer in use (and s_inv ready)
-    if (tid < 64) {
-      const float ph = __fmul_rn(float(pos), s_inv[tid]);
-      double sd, cd;
-      sincos(double(ph), &sd, &cd);
-      s_cos[tid] = __double2float_rn(cd);
-      s_sin[tid] = __double2float_rn(sd);
-    }
-    __syncthreads();
+    __syncwarp();  // the previous token's table is no longer read
+    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
+    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
+    __syncwarp();
     const size_t row = (size_t)b * Tmax + pos;
-    for (int u = tid; u < kRopeUnits + kVUnits; u += kRopeThreads) {
-      if (u < kRopeUnits) {
-        const int head = u >> 3, c = u & 7;  // pairs j = 8c .. 8c+7
-        const uint4* src;
-        uint4* dst;
-        if (head < kQHeads) {
-          src = q + ((size_t)tok * kQHeads + head) * 16;
-          dst = q_rot + ((size_t)tok * kQHeads + head) * 16;
-        } else {
-          const int g = head - kQHeads;
-          src = k + ((size_t)tok * kKVHeads + g) * 16;
-          dst = cache_k + (row * kKVHeads + g) * 16;
-        }
-        const uint4 x1 = __ldg(src + c);
-        const uint4 x2 = __ldg(src + c + 8);
-        uint4 y1, y2;
-        rotate8(x1, x2, s_cos + 8 * c, s_sin + 8 * c, y1, y2);
-        dst[c] = y1;
-        dst[c + 8] = y2;
-      } else {
-        const int w = u - kRopeUnits;
-        cache_v[row * (kKVHeads * 16) + w] = __ldg(v + (size_t)tok * (kKVHeads * 16) + w);
-      }
+    const uint4* qsrc = q + (size_t)tok * kQHeads * 16;
+    const uint4* ksrc = k + (size_t)tok * kKVHeads * 16;
+    uint4* qdst = q_rot + (size_t)tok * kQHeads * 16;
+    uint4* kdst = cache_k + row * kKVHeads * 16;
+    // 56 heads x 8 pair groups = 448 rotation units: unit u = head * 8 + c (pairs 8c .. 8c+7)
+    uint4 x1[14], x2[14];
+#pragma unroll
+    for (int m = 0; m < 14; ++m) {
+      if (m % team != member) continue;
+      const int u = lane + 32 * m, head = u >> 3, c = u & 7;
+      const uint4* src = head < kQHeads ? qsrc + head * 16 : ksrc + (head - kQHeads) * 16;
+      x1[m] = __ldg(src + c);
+      x2[m] = __ldg(src + c + 8);
     }
+    uint4 vv[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (m % team == member) vv[m] = __ldg(v + (size_t)tok * (kKVHeads * 16) + lane + 32 * m);
+#pragma unroll
+    for (int m = 0; m < 14; ++m) {
+      if (m % team != member) continue;
+      const int u = lane + 32 * m, head = u >> 3, c = u & 7;
+      uint4 y1, y2;
+      rotate8(x1[m], x2[m], &s_cos[warp][8 * c], &s_sin[warp][8 * c], y1, y2);
+      uint4* dst = head < kQHeads ? qdst + head * 16 : kdst + (head - kQHeads) * 16;
+      dst[c] = y1;
+      dst[c + 8] = y2;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (m % team == member) cache_v[row * (kKVHeads * 16) + lane + 32 * m] = vv[m];
   }
+}
+
+// The fp32 table the append kernel uses: entry (p, j) for positions
+// [p0, p0 + n) and frequencies j < 64.
+__global__ void rope_table_kernel(int p0, int n, float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)n * 64) return;
+  const int j = int(idx & 63);
+  const int pos = p0 + int(idx >> 6);
+  float c, s;
+  rope_cos_sin(__fmul_rn(float(pos), rope_inv_freq(j)), c, s);
+  cos_out[idx] = c;
+  sin_out[idx] = s;
 }
 
 }  // namespace grok
@@ -127,10 +208,32 @@ extern "C" grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* 
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
   const long long ntok = (long long)B * T;
-  const int grid = int(ntok < (long long)sms * 16 ? ntok : (long long)sms * 16);
-  rope_kv_append_kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  // warps per token: as many as keep about four resident CTAs' worth of warps per SM busy, up to 8
+  int team = 1;
+  while (team < 8 && ntok * team * 2 <= (long long)sms * 4 * kRopeWarps) team *= 2;
+  const long long want = (ntok * team + kRopeWarps - 1) / kRopeWarps;
+  const int grid = int(want < (long long)sms * 8 ? want : (long long)sms * 8);
+  auto kernel = team == 8 ? rope_kv_append_kernel<8>
+               : team == 4 ? rope_kv_append_kernel<4>
+               : team == 2 ? rope_kv_append_kernel<2>
+                           : rope_kv_append_kernel<1>;
+  kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
       start_pos, B, T, Tmax, reinterpret_cast<uint4*>(q_rot), reinterpret_cast<uint4*>(cache_k),
       reinterpret_cast<uint4*>(cache_v), dev_status);
   return check_launch("rope_kv_append");
+}
+
+extern "C" grok_status grok_rope_cos_sin(int first_position, int n_positions, float* cos_out, float* sin_out,
+                                         void* stream) {
+  if (!cos_out || !sin_out) return fail(GROK_ERR_INVALID_ARG, "grok_rope_cos_sin: null pointer");
+  if (first_position < 0 || n_positions < 1 || (long long)first_position + n_positions > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_rope_cos_sin: positions must lie in [0, %d)", GROK_MAX_POSITION);
+  int sms = 0;
+  grok_status st = device_sm_count(&sms);
+  if (st != GROK_OK) return st;
+  const long long total = (long long)n_positions * 64;
+  rope_table_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      first_position, n_positions, cos_out, sin_out);
+  return check_launch("rope_table");
 }

@@ -95,6 +95,15 @@ grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const gr
                                 grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status, void* stream);
 
 /*
+ * The fp32 RoPE table the append uses (ch. 4 §4.3.1: phase = t * inv_freq,
+ * cos and sin of it): cos_out[i * 64 + j] and sin_out[i * 64 + j] for position
+ * first_position + i and frequency j < 64, i < n_positions; each value is the
+ * correctly rounded fp32 cos / sin of the fp32 phase RN32(p * inv_freq[j]).
+ * cos_out, sin_out: device float[n_positions * 64]. Positions < GROK_MAX_POSITION.
+ */
+grok_status grok_rope_cos_sin(int first_position, int n_positions, float* cos_out, float* sin_out, void* stream);
+
+/*
  * Prefill attention of T new tokens per sequence over the appended cache
  * (ch. 4 §4.5.2-§4.5.4, ch. 6 §6.4.2).
  *

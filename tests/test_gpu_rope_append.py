@@ -66,3 +66,15 @@ def test_append_host_argument_checks():
     mis = flat[1:].view(q.shape)              # 2-byte offset: not 16-byte aligned
     with pytest.raises(G.GrokError):
         G.rope_kv_append(q, k, v, start, mis, ck, cv)
+
+
+def test_cos_sin_table_bit_exact_for_every_supported_position():
+    """All 65536 positions x 64 frequencies of the device table equal the oracle's fp32 values."""
+    import grok_gqa_attention_gb300 as G
+    from oracle import rope as R
+    c, s = G.rope_cos_sin(0, R.MAX_POSITION)
+    torch.cuda.synchronize()
+    t = np.arange(R.MAX_POSITION, dtype=np.float32)[None, :]
+    oc, os_ = R.cos_sin(R.phase(t, R.inv_freq(128)))
+    assert np.array_equal(c.cpu().numpy().view(np.uint32), oc[0].view(np.uint32))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_[0].view(np.uint32))
