@@ -6,11 +6,11 @@
 // rotated with offset = step before the cache write; V written unrotated;
 // update_into at step[b]).
 //
-// One warp handles one token (b, i): its lanes evaluate the 64 (cos, sin)
-// pairs of the token's position in fp64 and round them to fp32; then the warp
-// streams the token's 48 query heads and 8 key heads (128-bit loads of 8 bf16
-// of the first half and the matching 8 of the second half) and its 8 value
-// heads. The rotation uses separately rounded fp32 multiplies and adds
+// A team of 1, 2, 4 or 8 warps handles one token (b, i) (more warps per token
+// when there are few tokens): each warp evaluates the 64 (cos, sin) pairs of
+// the token's position in fp64 and rounds them to fp32, then streams its share
+// of the token's 48 query heads and 8 key heads (128-bit loads of 8 bf16 of the
+// first half and the matching 8 of the second half) and of its 8 value heads. The rotation uses separately rounded fp32 multiplies and adds
 // (no FMA contraction), so the result is bit-for-bit the fp32 chain.
 //
 // Memory-bound: per token it reads 14 KB (q, k, v) and writes 14 KB.
