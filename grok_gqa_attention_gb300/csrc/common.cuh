@@ -296,6 +296,35 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   return r;
 }
 
+// 2^x for a pair of x in [-126, 0] on the FMA pipe instead of the special-
+// function unit: x = j + f with j the nearest integer (rounded by adding
+// 1.5 * 2^23, so j lands in the low mantissa bits of the sum) and f in
+// [-1/2, 1/2]; 2^f from a degree-4 polynomial fitted here for relative error
+// on [-1/2, 1/2] (weighted least squares refined toward equal ripple, then
+// rounded to fp32: maximum relative error 2.7e-6 including the fp32 Horner
+// steps); 2^j added to the exponent field. A NaN input need not give NaN.
+__device__ __forceinline__ void exp2_poly_f2(uint64_t x, float& y0, float& y1) {
+  const uint64_t big = f2_pack(12582912.0f, 12582912.0f);
+  const uint64_t t = f2_add(x, big);
+  const uint64_t f = f2_sub(x, f2_sub(t, big));
+  uint64_t q = f2_fma(f2_pack(0x1.3997ca0p-7f, 0x1.3997ca0p-7f), f, f2_pack(0x1.ca14400p-5f, 0x1.ca14400p-5f));
+  q = f2_fma(q, f, f2_pack(0x1.ec06da0p-3f, 0x1.ec06da0p-3f));
+  q = f2_fma(q, f, f2_pack(0x1.62e0dc0p-1f, 0x1.62e0dc0p-1f));
+  q = f2_fma(q, f, f2_pack(0x1.ffffe80p-1f, 0x1.ffffe80p-1f));
+  float t0, t1, q0, q1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(q, q0, q1);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
+// One lane of a converged warp (the same lane every time it is called).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
+
 // ----------------------------------------------------------------------------
 // bf16 packing: cvt.rn.bf16x2.f32 d, a, b puts a in the upper half, b in the lower.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

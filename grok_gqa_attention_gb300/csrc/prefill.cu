@@ -6,36 +6,47 @@
 // sum of V); ch. 6 "model.py close reading II", §6.4.2 (causal x padding mask).
 //
 // Work item = (sequence b, 128-row query tile, KV group g, pair of query heads
-// of that group). One persistent CTA per SM walks the items, heaviest first.
-// Both heads of an item read the same K/V tiles, so every K/V tile staged in
-// shared memory by TMA feeds two heads; the three head pairs of a group run in
-// neighbouring CTAs and meet the same tiles in L2.
+// of that group). One persistent CTA per SM walks the items in a snake order
+// over rounds of gridDim.x items (heaviest first; odd rounds reversed), which
+// evens out the causal work per CTA. Both heads of an item read the same K/V
+// tiles, so every K/V tile staged in shared memory by TMA feeds two heads; the
+// three head pairs of a group run in neighbouring CTAs and meet the same tiles
+// in L2.
+//
+// Four independent chains per CTA. Each 128-key tile of each head is handled
+// as two 64-key halves, and each (head, half) is its own chain:
+//   S_h = Q K_h^T (64 TMEM columns) -> softmax -> P_h over S_h ->
+//   O += P_h V_h, then at once S_h of the next tile = Q K_h'^T
+// so one half's softmax overlaps the other half's products. The next tile's
+// first product is issued right after the previous P V that read the same
+// columns (the tensor pipe runs one thread's MMAs in order).
 //
 // Warp roles (608 threads):
 //   warp 0      TMA producer: Q tiles of both heads, then K and V tiles in two
-//               separate 2-stage rings (a K tile is released as soon as both
-//               heads' Q K^T products finish, a tile ahead of its V tile)
-//   warp 1      TMEM owner and MMA issuer of head slot 0 (one thread)
-//   warp 18     MMA issuer of head slot 1 (one thread, on another SMSP). The
-//               two issuers pass a token so the tensor queue alternates
-//               slot 0 / slot 1 per key tile (one slot's softmax then overlaps
-//               the other's products), while each issuer's waits and commits
-//               overlap the other's issue window.
-//   warps 2-9   softmax + epilogue for head slot 0: warps 2-5 convert key
-//               columns 0..63 and write output features 0..63, warps 6-9
-//               columns 64..127 and features 64..127 (warp w reads TMEM lanes
-//               32 (w % 4) .. +31, so four consecutive warps cover rows 0..127)
+//               separate 2-stage rings
+//   warp 1      TMEM owner and MMA issuer of head slot 0
+//   warp 18     MMA issuer of head slot 1 (on another SMSP). Each issuer warp
+//               runs converged through its barrier waits and one fixed lane
+//               issues the MMAs and commits; the two issuers do not coordinate,
+//               so one's waits are covered by the other's products.
+//   warps 2-9   softmax + epilogue for head slot 0: warps 2-5 own half 0 (key
+//               columns 0..63 of each tile, output features 0..63), warps 6-9
+//               half 1 (warp w reads TMEM lanes 32 (w % 4) .. +31, so four
+//               consecutive warps cover rows 0..127)
 //   warps 10-17 the same for head slot 1
-// Four softmax warps per SMSP hide the latency of the special-function chain;
-// the two halves of a row add their partial row sums through shared memory.
-// TMEM (512 columns): per slot, S = Q K^T in 128 fp32 columns and O in 128.
-// The softmax warps overwrite S in place with P as two bf16 halves (hi, lo)
-// that sum to P to ~2^-16; O += P_hi V + P_lo V reads them straight from TMEM.
+// The two halves of a row add their partial row sums through shared memory.
+// TMEM (512 columns): per slot, S in 128 fp32 columns (half h in 64h..64h+63)
+// and O in 128. The softmax warps overwrite S in place with P as two bf16
+// halves (hi, lo) that sum to P to ~2^-16; O += P_hi V + P_lo V reads them
+// straight from TMEM.
 //
 // Softmax without a running maximum: every capped logit is below 30, so the
 // weights exp(c - 30) lie in (e^-60, 1] and fp32 holds them and their sums
 // with full relative precision. O therefore accumulates across all key tiles
-// with no rescaling; the epilogue divides by the row sum once.
+// with no rescaling; the epilogue divides by the row sum once. The weight's
+// tanh runs on the special-function unit; its exp2 does too for half of the
+// columns and runs as a polynomial on the FMA pipe for the other half, which
+// balances the two pipes.
 //
 // Keys beyond the last visible row of an item's final tile may hold anything
 // (including NaN): the softmax gives them weight 0 by selection and the softmax
@@ -57,9 +68,8 @@ constexpr int kPfData = kQBytes + 2 * kPfStages * kTileBytes;
 struct PfBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
-  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t s_full[2][2], p_full[2][2], o_full[2], o_empty[2];  // [slot][half]
   uint64_t mma_done;
-  uint64_t issue_turn[2];  // the issuers alternate: slot 0's tile-j MMAs, then slot 1's
   uint64_t lsum_ready[2];  // both halves of a slot posted their partial row sums
   float lsum[2][2][2][128];  // [item parity][slot][half][row]
   uint32_t tmem_base;
@@ -80,8 +90,18 @@ struct PfItem {
   int s, n;     // start position, valid length
   int kv_end;   // keys [0, kv_end) are visible to some row of the tile
   int n_kv;     // key tiles to visit (0: skip the item)
+  int n_sub;    // 64-key halves of those tiles that hold a visible key
   int bad;      // GROK_DEV_* bits when the sequence's integers are invalid
 };
+
+// The item a CTA takes in round rd (-1 when there is none): rounds of gridDim.x
+// items, odd rounds in reverse CTA order, so the heavy items of one round and
+// the light items of the next land on the same CTA.
+__device__ __forceinline__ int pf_item_index(const PfParams& p, int rd) {
+  const int k = (rd & 1) ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
+  const long long item = (long long)rd * gridDim.x + k;
+  return item < p.n_items ? int(item) : -1;
+}
 
 __device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
   PfItem it;
@@ -99,11 +119,13 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
   if (it.bad) {
     it.kv_end = 0;
     it.n_kv = 0;
+    it.n_sub = 0;
     return it;
   }
   const int last_row = min(it.qt * kPfRows + kPfRows, p.T);  // rows [qt*128, last_row)
   it.kv_end = min(it.s + last_row, it.s + it.n);
-  it.n_kv = (it.kv_end + kPfKeys - 1) / kPfKeys;
+  it.n_sub = (it.kv_end + 63) / 64;
+  it.n_kv = (it.n_sub + 1) / 2;
   return it;
 }
 
@@ -123,35 +145,58 @@ __device__ __forceinline__ void pf_issue_qk(uint32_t d, uint64_t qdesc, uint64_t
   }
 }
 
-__device__ __forceinline__ void pf_issue_pv(uint32_t d, uint32_t pbase, uint64_t vdesc, bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kD, 1);  // V is N(d)-contiguous
+// Q K^T for one 64-key half of a K tile (kdesc already points at its first row).
+__device__ __forceinline__ void pf_issue_qk_half(uint32_t d, uint64_t qdesc, uint64_t kdesc) {
+  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, 64, 0);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
-    // P for keys 32c..32c+31: hi in columns 32c..32c+15, lo in 32c+16..32c+31
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t off = uint64_t(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+    umma_ss(d, qdesc + off, kdesc + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V over the keys 64h .. 64h+63 of a tile.
+__device__ __forceinline__ void pf_issue_pv_half(uint32_t d, uint32_t pbase, uint64_t vdesc, int h, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kD, 1);
+#pragma unroll
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = 4 * h + k4;
     const uint32_t pcol = (kk >> 1) * 32 + (kk & 1) * 8;
     const uint64_t b = vdesc + uint64_t((kk * 2048) >> 4);
-    umma_ts(d, pbase + pcol, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(d, pbase + pcol, b, idesc, (accumulate || k4 > 0) ? 1u : 0u);
     umma_ts(d, pbase + pcol + 16, b, idesc, 1u);
   }
 }
 
+// Column pairs of a 32-key chunk whose exp2 runs on the FMA pipe (bit e: pair
+// e); the rest use the special-function unit, which also evaluates every tanh.
+constexpr uint32_t kPolyPairs = 0x3333;
+
 // S -> P for one 32-key chunk c of one row (this thread's TMEM lane): weights
-// exp(c - 30), zero where masked, accumulated into the row sum and returned as
-// bf16 hi/lo halves for the caller to write back over S (keys 32c..32c+31: hi in
-// columns 32c..32c+15, lo in 32c+16..32c+31).
+// exp(capped logit - 30), zero where masked, accumulated into the row sum and
+// returned as bf16 hi/lo halves for the caller to write back over S (keys
+// 32c..32c+31: hi in columns 32c..32c+15, lo in 32c+16..32c+31).
 template <bool kMask>
 __device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c, int rel, float& l0, float& l1,
                                                  uint32_t (&hi)[16], uint32_t (&lo)[16]) {
-  // The scalar arithmetic of capped_weight and split_bf16x2, two columns at a
-  // time with packed f32x2 instructions (identical results, fewer issue slots).
+  // The arithmetic of capped_weight and split_bf16x2, two columns at a time
+  // with packed f32x2 instructions; the exp2 of the pairs in kPolyPairs is the
+  // FMA-pipe polynomial instead of ex2.approx.
   const uint64_t y2 = f2_pack(kY, kY), t2 = f2_pack(kT, kT), mt2 = f2_pack(-kT, -kT);
   uint64_t l = f2_pack(l0, l1);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float y0, y1, x0, x1;
     f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), y2), y0, y1);
-    f2_unpack(f2_fma(f2_pack(tanh_approx(y0), tanh_approx(y1)), t2, mt2), x0, x1);
-    float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
+    const uint64_t x = f2_fma(f2_pack(tanh_approx(y0), tanh_approx(y1)), t2, mt2);
+    float w0, w1;
+    if ((kPolyPairs >> e) & 1) {
+      exp2_poly_f2(x, w0, w1);
+    } else {
+      f2_unpack(x, x0, x1);
+      w0 = ex2_approx(x0);
+      w1 = ex2_approx(x1);
+    }
     if (kMask) {
       w0 = (c * 32 + 2 * e <= rel) ? w0 : 0.f;
       w1 = (c * 32 + 2 * e + 1 <= rel) ? w1 : 0.f;
@@ -205,15 +250,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars->v_empty[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 256);
+      mbar_init(&bars->s_full[s][0], 1);
+      mbar_init(&bars->s_full[s][1], 1);
+      mbar_init(&bars->p_full[s][0], 128);
+      mbar_init(&bars->p_full[s][1], 128);
       mbar_init(&bars->o_full[s], 1);
       mbar_init(&bars->o_empty[s], 256);
       mbar_init(&bars->lsum_ready[s], 256);
     }
     mbar_init(&bars->mma_done, 2);
-    mbar_init(&bars->issue_turn[0], 1);
-    mbar_init(&bars->issue_turn[1], 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -235,7 +280,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int kv_it = 0, q_it = 0;
-      for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+      for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
         const PfItem it = pf_item(p, item);
         if (it.n_kv == 0) continue;
         if (!mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort, p.status)) break;
@@ -276,74 +321,93 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (q_it > 0) mbar_wait(&bars->q_full, (q_it - 1) & 1, &never, p.status);
     }
   } else if (warp == 1 || warp == 18) {
-    // ------------------------------------------------------------ MMA issuers (one per slot)
-    if (lane == 0) {
-      const int slot = warp == 1 ? 0 : 1;
-      const uint32_t s_tm = tmem + slot * 256, o_tm = s_tm + 128;
-      const uint64_t qd = make_sdesc_sw128(smem_u32(sQ), 16, 1024) + slot * kQSlotDesc;
-      const uint64_t kd = make_sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vd = make_sdesc_sw128(smem_u32(sV), kBox, 1024);
-      int kv_it = 0, q_it = 0, item_it = 0;
-      int turns = 0;  // turns taken by this issuer; slot 0 starts
-      bool ok = true;
-      auto take_turn = [&]() -> bool {
-        const uint32_t par = uint32_t(turns & 1) ^ (slot == 0 ? 1u : 0u);
-        return mbar_wait(&bars->issue_turn[slot], par, abort, p.status);
-      };
-      auto pass_turn = [&]() {
-        mbar_arrive(&bars->issue_turn[slot ^ 1]);
-        ++turns;
-      };
-      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        const PfItem it = pf_item(p, item);
-        if (it.n_kv == 0) continue;
-        if (!mbar_wait(&bars->q_full, q_it & 1, abort, p.status)) break;
-        {
-          const int st = kv_it % kPfStages;
-          if (!mbar_wait(&bars->k_full[st], (kv_it / kPfStages) & 1, abort, p.status) || !take_turn()) break;
-          tc_fence_after();
-          pf_issue_qk(s_tm, qd, kd + st * kStageDesc);
-          pass_turn();
-          umma_commit(&bars->s_full[slot]);
+    // ------------------------------------------------------------ MMA issuers (one warp per slot)
+    // The warp runs converged through the waits; one fixed lane issues every
+    // MMA and commit (a commit tracks the MMAs of the thread that issues it).
+    const bool leader = elect_one();
+    const int slot = warp == 1 ? 0 : 1;
+    const uint32_t s_tm = tmem + slot * 256, o_tm = s_tm + 128;
+    const uint64_t qd = make_sdesc_sw128(smem_u32(sQ), 16, 1024) + slot * kQSlotDesc;
+    const uint64_t kd = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t vd = make_sdesc_sw128(smem_u32(sV), kBox, 1024);
+    int kv_it = 0, q_it = 0, item_it = 0;
+    int pc0 = 0, pc1 = 0;  // P hand-overs consumed per half (p_full parity)
+    bool ok = true;
+    for (int rd = 0, item; ok && (item = pf_item_index(p, rd)) >= 0; ++rd) {
+      const PfItem it = pf_item(p, item);
+      if (it.n_kv == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, q_it & 1, abort, p.status))) break;
+      {
+        const int st = kv_it % kPfStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (kv_it / kPfStages) & 1, abort, p.status))) break;
+        tc_fence_after();
+        if (leader) {
+          if (it.n_sub >= 2)
+            pf_issue_qk(s_tm, qd, kd + st * kStageDesc);
+          else
+            pf_issue_qk_half(s_tm, qd, kd + st * kStageDesc);
+          umma_commit(&bars->s_full[slot][0]);
+          if (it.n_sub >= 2) umma_commit(&bars->s_full[slot][1]);
           umma_commit(&bars->k_empty[st]);
         }
-        for (int j = 0; j < it.n_kv; ++j) {
-          const int cur = kv_it + j;
-          const int st = cur % kPfStages;
-          const bool has_next = j + 1 < it.n_kv;
-          const int stn = (cur + 1) % kPfStages;
-          // Every wait that is normally already satisfied comes first; the wait
-          // for this slot's P, the real dependency, comes last so that only it
-          // (about 100 cycles even when ready) sits between P and the products.
-          if (!mbar_wait(&bars->v_full[st], (cur / kPfStages) & 1, abort, p.status) ||
-              (has_next && !mbar_wait(&bars->k_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status)) ||
-              (j == 0 && !mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status)) ||
-              !take_turn() || !mbar_wait(&bars->p_full[slot], cur & 1, abort, p.status)) {
+        __syncwarp();
+        // The first tile's other inputs, waited while that product runs.
+        const bool w = mbar_wait(&bars->v_full[st], (kv_it / kPfStages) & 1, abort, p.status) &&
+                       (it.n_sub <= 2 || mbar_wait(&bars->k_full[(kv_it + 1) % kPfStages], ((kv_it + 1) / kPfStages) & 1, abort, p.status)) &&
+                       mbar_wait(&bars->o_empty[slot], (item_it & 1) ^ 1, abort, p.status);
+        if (!__all_sync(0xffffffffu, w)) break;
+      }
+      for (int u = 0; u < it.n_sub; ++u) {
+        const int h = u & 1, j = u >> 1;
+        const int cur = kv_it + j;
+        const int st = cur % kPfStages, stn = (cur + 1) % kPfStages;
+        const bool qk_next = u + 2 < it.n_sub;
+        const bool tile_end = h == 1 || u == it.n_sub - 1;
+        // V of tile j and K of tile j + 1 were waited for earlier (item start or
+        // the middle of the previous tile's second step); only P is waited here.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->p_full[slot][h], uint32_t(h ? pc1 : pc0) & 1, abort, p.status))) {
+          ok = false;
+          break;
+        }
+        if (h) ++pc1; else ++pc0;
+        tc_fence_after();
+        if (leader) pf_issue_pv_half(o_tm, s_tm, vd + st * kStageDesc, h, u > 0);
+        __syncwarp();
+        if (h == 1 && u + 1 < it.n_sub) {
+          // inputs of the next tile's steps: its V and the K after it
+          const bool w = mbar_wait(&bars->v_full[stn], ((cur + 1) / kPfStages) & 1, abort, p.status) &&
+                         (u + 3 >= it.n_sub || mbar_wait(&bars->k_full[st], ((cur + 2) / kPfStages) & 1, abort, p.status));
+          if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          pf_issue_pv(o_tm, s_tm, vd + st * kStageDesc, j > 0);
-          if (has_next) pf_issue_qk(s_tm, qd, kd + stn * kStageDesc);
-          pass_turn();
-          umma_commit(&bars->v_empty[st]);
-          if (has_next) {
-            umma_commit(&bars->s_full[slot]);
-            umma_commit(&bars->k_empty[stn]);
-          } else {
+        }
+        if (leader) {
+          if (qk_next) {
+            pf_issue_qk_half(s_tm + 64 * h, qd, kd + stn * kStageDesc + uint64_t((8192 * h) >> 4));
+            umma_commit(&bars->s_full[slot][h]);
+          }
+          if (tile_end) {
+            umma_commit(&bars->v_empty[st]);
+            if (j + 1 < it.n_kv) umma_commit(&bars->k_empty[stn]);
+          }
+          if (u == it.n_sub - 1) {
             umma_commit(&bars->o_full[slot]);
             umma_commit(&bars->q_empty);
           }
         }
-        kv_it += it.n_kv;
-        ++q_it;
-        ++item_it;
+        __syncwarp();
       }
-      // No MMA may still be running when TMEM is released.
-      umma_commit(&bars->mma_done);
-      volatile int never = 0;
-      mbar_wait(&bars->mma_done, 0, &never, p.status);
+      kv_it += it.n_kv;
+      ++q_it;
+      ++item_it;
     }
+    // No MMA may still be running when TMEM is released.
+    if (leader) umma_commit(&bars->mma_done);
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(&bars->mma_done, 0, &never, p.status);
   } else if (warp >= 2 && warp <= 17) {
     // ------------------------------------------------------------ softmax + epilogue
     const int slot = (warp - 2) >> 3;
@@ -351,8 +415,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // query row within the tile
     const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
-    int tile_cnt = 0, item_it = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    int tile_cnt = 0, item_it = 0, sub_cnt = 0;
+    for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
       const PfItem it = pf_item(p, item);
       if (it.n_kv == 0) {
         if (it.bad && slot == 0 && half == 0 && r == 0) report(p.status, it.bad);
@@ -362,8 +426,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int lim = min(it.s + i, it.s + it.n - 1);  // last visible key of this row
       float l0 = 0.f, l1 = 0.f;
       bool ok = true;
-      for (int j = 0; j < it.n_kv; ++j) {
-        ok = mbar_wait(&bars->s_full[slot], (tile_cnt + j) & 1, abort, p.status);
+      for (int u = half; u < it.n_sub; u += 2) {
+        const int j = u >> 1;
+        ok = mbar_wait(&bars->s_full[slot][half], sub_cnt & 1, abort, p.status);
+        ++sub_cnt;
         if (!__all_sync(0xffffffffu, ok)) {  // leave together: the TMEM ops below are warp-collective
           ok = false;
           break;
@@ -372,11 +438,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int rel = lim - j * kPfKeys;       // columns c <= rel are visible
         // The choice must be warp-uniform: the TMEM loads and stores inside
         // are warp-collective (.sync.aligned).
-        if (__all_sync(0xffffffffu, rel >= kPfKeys - 1))
+        if (__all_sync(0xffffffffu, rel >= 64 * half + 63))
           pf_softmax_half<false>(trow, half, rel, l0, l1);
         else
           pf_softmax_half<true>(trow, half, rel, l0, l1);
-        if (half == 0 && j == it.n_kv - 1) {
+        if (u == it.n_sub - 1) {
           // Zero the V rows of the last tile that lie beyond every visible key.
           // Both slots do it (same zeros) before handing over their P, since
           // each slot's PV product may be issued first.
@@ -396,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[slot]);
+        mbar_arrive(&bars->p_full[slot][half]);
       }
       if (!ok) break;
       tile_cnt += it.n_kv;
