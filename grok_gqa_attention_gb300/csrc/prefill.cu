@@ -64,6 +64,7 @@ constexpr int kBox = 128 * 128;             // [128 rows][64 bf16], 128-byte swi
 constexpr int kQBytes = 2 * 2 * kBox;       // two heads, two 64-wide halves of d
 constexpr int kTileBytes = 2 * kBox;        // one K or V tile: two 64-wide halves of d
 constexpr int kPfData = kQBytes + 2 * kPfStages * kTileBytes;
+constexpr int kPfSeqCache = 512;  // sequences whose start / valid length are staged in shared memory
 
 struct PfBars {
   uint64_t q_full, q_empty;
@@ -71,7 +72,9 @@ struct PfBars {
   uint64_t s_full[2][2], p_full[2][2], o_full[2], o_empty[2];  // [slot][half]
   uint64_t mma_done;
   uint64_t lsum_ready[2];  // both halves of a slot posted their partial row sums
+  uint64_t epi_done[2];    // the slot's eight epilogue warps' output stores have read their staging
   float lsum[2][2][2][128];  // [item parity][slot][half][row]
+  int seq_start[kPfSeqCache], seq_valid[kPfSeqCache];
   uint32_t tmem_base;
   int abort;
 };
@@ -81,7 +84,6 @@ struct PfParams {
   int B, T, Tmax, n_qt, n_items;
   const int32_t* start_pos;
   const int32_t* valid_len;
-  uint4* out;
   int32_t* status;
 };
 
@@ -103,7 +105,7 @@ __device__ __forceinline__ int pf_item_index(const PfParams& p, int rd) {
   return item < p.n_items ? int(item) : -1;
 }
 
-__device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
+__device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars, int item) {
   PfItem it;
   it.hp = item % 3;
   int rest = item / 3;
@@ -111,8 +113,13 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, int item) {
   rest /= kKVHeads;
   it.b = rest % p.B;
   it.qt = p.n_qt - 1 - rest / p.B;  // heaviest (last) query tiles first
-  it.s = __ldg(p.start_pos + it.b);
-  it.n = p.valid_len ? __ldg(p.valid_len + it.b) : p.T;
+  if (it.b < kPfSeqCache) {
+    it.s = bars->seq_start[it.b];
+    it.n = bars->seq_valid[it.b];
+  } else {
+    it.s = __ldg(p.start_pos + it.b);
+    it.n = p.valid_len ? __ldg(p.valid_len + it.b) : p.T;
+  }
   it.bad = 0;
   if (it.s < 0 || (long long)it.s + p.T > p.Tmax) it.bad |= GROK_DEV_BAD_START;
   if (it.n < 1 || it.n > p.T) it.bad |= GROK_DEV_BAD_VALID;
@@ -230,7 +237,8 @@ __device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PfParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const PfParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -257,15 +265,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars->o_full[s], 1);
       mbar_init(&bars->o_empty[s], 256);
       mbar_init(&bars->lsum_ready[s], 256);
+      mbar_init(&bars->epi_done[s], 8);
     }
     mbar_init(&bars->mma_done, 2);
     bars->abort = 0;
     fence_barrier_init();
   }
+  // Every role reads each item's sequence integers; stage them once.
+  for (int b = threadIdx.x; b < p.B && b < kPfSeqCache; b += blockDim.x) {
+    bars->seq_start[b] = __ldg(p.start_pos + b);
+    bars->seq_valid[b] = p.valid_len ? __ldg(p.valid_len + b) : p.T;
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -281,7 +296,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       int kv_it = 0, q_it = 0;
       for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
-        const PfItem it = pf_item(p, item);
+        const PfItem it = pf_item(p, bars, item);
         if (it.n_kv == 0) continue;
         if (!mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort, p.status)) break;
         mbar_arrive_expect_tx(&bars->q_full, kQBytes);
@@ -334,7 +349,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int pc0 = 0, pc1 = 0;  // P hand-overs consumed per half (p_full parity)
     bool ok = true;
     for (int rd = 0, item; ok && (item = pf_item_index(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item(p, item);
+      const PfItem it = pf_item(p, bars, item);
       if (it.n_kv == 0) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, q_it & 1, abort, p.status))) break;
       {
@@ -348,7 +363,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             pf_issue_qk_half(s_tm, qd, kd + st * kStageDesc);
           umma_commit(&bars->s_full[slot][0]);
           if (it.n_sub >= 2) umma_commit(&bars->s_full[slot][1]);
-          umma_commit(&bars->k_empty[st]);
+          // (the last tile's K and V stages are handed back by the epilogue, which
+          // stages the output in them)
+          if (it.n_kv > 1) umma_commit(&bars->k_empty[st]);
+          if (it.n_sub <= 2) umma_commit(&bars->q_empty);  // Q is read by no later product
         }
         __syncwarp();
         // The first tile's other inputs, waited while that product runs.
@@ -387,15 +405,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (qk_next) {
             pf_issue_qk_half(s_tm + 64 * h, qd, kd + stn * kStageDesc + uint64_t((8192 * h) >> 4));
             umma_commit(&bars->s_full[slot][h]);
+            // The item's last Q K^T: the producer may load the next item's Q
+            // while the remaining P V products and the epilogue run.
+            if (u + 3 == it.n_sub) umma_commit(&bars->q_empty);
           }
-          if (tile_end) {
+          if (tile_end && j + 1 < it.n_kv) {  // not the item's last tile
             umma_commit(&bars->v_empty[st]);
-            if (j + 1 < it.n_kv) umma_commit(&bars->k_empty[stn]);
+            if (j + 2 < it.n_kv) umma_commit(&bars->k_empty[stn]);
           }
-          if (u == it.n_sub - 1) {
-            umma_commit(&bars->o_full[slot]);
-            umma_commit(&bars->q_empty);
-          }
+          if (u == it.n_sub - 1) umma_commit(&bars->o_full[slot]);
         }
         __syncwarp();
       }
@@ -417,7 +435,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
     int tile_cnt = 0, item_it = 0, sub_cnt = 0;
     for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item(p, item);
+      const PfItem it = pf_item(p, bars, item);
       if (it.n_kv == 0) {
         if (it.bad && slot == 0 && half == 0 && r == 0) report(p.status, it.bad);
         continue;
@@ -469,14 +487,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // row sum of both halves (double-buffered by item parity)
       bars->lsum[item_it & 1][slot][half][r] = l0 + l1;
       mbar_arrive(&bars->lsum_ready[slot]);
-      // epilogue: O / l -> bf16 for this half's 64 output features
+      // Epilogue: O / l -> bf16 for this half's 64 output features, staged in
+      // shared memory (128-byte swizzled, as TMA expects) and written by TMA, so
+      // the scattered rows do not pass through the load/store unit. The staging
+      // buffers are the item's last K stage (slot 0) and V stage (slot 1): every
+      // product of both slots has read them once both slots' O are complete.
       ok = mbar_wait(&bars->lsum_ready[slot], item_it & 1, abort, p.status) &&
-           mbar_wait(&bars->o_full[slot], item_it & 1, abort, p.status);
+           mbar_wait(&bars->o_full[0], item_it & 1, abort, p.status) &&
+           mbar_wait(&bars->o_full[1], item_it & 1, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const float inv_l = 1.0f / (bars->lsum[item_it & 1][slot][0][r] + bars->lsum[item_it & 1][slot][1][r]);
       const int h = it.g * kGroup + it.hp * 2 + slot;
-      uint4* dst = p.out + (((size_t)it.b * p.T + i) * kQHeads + h) * 16 + half * 8;
+      const int st_last = (tile_cnt - 1) % kPfStages;
+      uint8_t* stage = (slot == 0 ? sK : sV) + st_last * kTileBytes + half * kBox;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t ov[32];
@@ -486,16 +510,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
-        if (i < p.T) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[cc * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) {
+          const int c = cc * 4 + q;  // 16-byte chunk of the row's 128 bytes
+          *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_empty[slot]);
+      mbar_arrive(&bars->o_empty[slot]);  // O is read: the next item's products may overwrite it
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = it.qt * kPfRows + quad * 32;
+        if (row0 < p.T) {
+          tma_store_4d(&tm_o, stage + quad * 32 * 128, half * 64, h, row0, it.b);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&bars->epi_done[slot]);
+        // One thread per slot hands the two staging stages back to the producer
+        // once all eight of the slot's stores have read them (each stage needs
+        // one hand-back from each slot).
+        if (half == 0 && quad == 2) {
+          if (mbar_wait(&bars->epi_done[slot], item_it & 1, abort, p.status)) {
+            mbar_arrive(&bars->k_empty[st_last]);
+            mbar_arrive(&bars->v_empty[st_last]);
+          }
+        }
+      }
+      __syncwarp();
       ++item_it;
     }
+    if (lane == 0) bulk_wait_all();  // output stores complete before the CTA exits
   }
 
   __syncwarp();
@@ -526,12 +573,14 @@ extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint32_t box[4] = {64, 1, 128, 1};
   {
     const uint64_t dims[4] = {kD, kQHeads, uint64_t(T), uint64_t(B)};
     const uint64_t strides[3] = {kD * 2, uint64_t(kQHeads) * kD * 2, uint64_t(T) * kQHeads * kD * 2};
     if ((st = encode_tmap_bf16_4d(&tq, q_rot, dims, strides, box)) != GROK_OK) return st;
+    const uint32_t obox[4] = {64, 1, 32, 1};  // one epilogue warp's 32 rows x 64 features
+    if ((st = encode_tmap_bf16_4d(&to, out, dims, strides, obox)) != GROK_OK) return st;
   }
   {
     const uint64_t dims[4] = {kD, kKVHeads, uint64_t(Tmax), uint64_t(B)};
@@ -547,7 +596,6 @@ extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16
   prm.n_items = prm.n_qt * B * kKVHeads * 3;
   prm.start_pos = start_pos;
   prm.valid_len = valid_len;
-  prm.out = reinterpret_cast<uint4*>(out);
   prm.status = dev_status;
 
   static bool attr_set = false;  // idempotent: every thread would set the same value
@@ -557,6 +605,6 @@ extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16
     attr_set = true;
   }
   const int grid = prm.n_items < sms ? prm.n_items : sms;
-  prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, prm);
+  prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
   return check_launch("prefill");
 }

@@ -17,6 +17,9 @@ SMALL_CASES = {
     "valid_len_edges": lambda: W.custom(B=3, T=130, Tmax=1000, start_pos=[0, 500, 870], valid_len=[1, 130, 64],
                                         seed=14),
     "many_tiles": lambda: W.custom(B=1, T=1000, Tmax=1100, start_pos=[100], valid_len=[999], seed=15),
+    # more sequences than the kernel stages in shared memory (512): the rest are read from global memory
+    "many_sequences": lambda: W.custom(B=520, T=8, Tmax=24, start_pos=[(7 * b) % 17 for b in range(520)],
+                                       valid_len=[1 + (5 * b) % 8 for b in range(520)], seed=16),
 }
 
 
