@@ -38,6 +38,10 @@ EXPORTS = (
     "grok_attn_combine",
     "grok_attn_decode_step_static",
     "grok_selftest_bounded_wait",
+    "grok_prefill_pipe_create",
+    "grok_prefill_pipe_submit",
+    "grok_prefill_pipe_wait",
+    "grok_prefill_pipe_destroy",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -78,6 +82,14 @@ def load() -> ctypes.CDLL:
     lib.grok_selftest_bounded_wait.argtypes = [P, P, ctypes.c_longlong, P]
     lib.grok_attn_decode_step_static.restype = I
     lib.grok_attn_decode_step_static.argtypes = [P, P, P, P, I, I, P, P, P]
+    lib.grok_prefill_pipe_create.restype = I
+    lib.grok_prefill_pipe_create.argtypes = [I, I, I, P, P, ctypes.POINTER(P)]
+    lib.grok_prefill_pipe_submit.restype = I
+    lib.grok_prefill_pipe_submit.argtypes = [P, P, P, P, P, P, P]
+    lib.grok_prefill_pipe_wait.restype = I
+    lib.grok_prefill_pipe_wait.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+    lib.grok_prefill_pipe_destroy.restype = I
+    lib.grok_prefill_pipe_destroy.argtypes = [P]
     _lib = lib
     return lib
 
@@ -227,3 +239,49 @@ def decode_step(q_rot, cache_k, cache_v, kv_len, workspace, out, dev_status=None
     """decode() then combine() on the same stream."""
     decode(q_rot, cache_k, cache_v, kv_len, workspace, dev_status, stream)
     combine(workspace, kv_len, out, cache_k.shape[1], dev_status, stream)
+
+
+def _want_host(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill_pipe_create(B: int, T: int, Tmax: int, cache_k, cache_v) -> ctypes.c_void_p:
+    """A host-buffer prefill pipeline over the device caches (see grok_prefill_pipe_create)."""
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    h = ctypes.c_void_p()
+    _check(load().grok_prefill_pipe_create(int(B), int(T), int(Tmax), _ptr(cache_k), _ptr(cache_v), ctypes.byref(h)))
+    return h
+
+
+def prefill_pipe_submit(pipe, B: int, T: int, q, k, v, start_pos, valid_len, out) -> None:
+    """Queue one step from host tensors (page-locked for overlap); out is written by the next wait."""
+    _want_host(q, "q", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want_host(k, "k", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want_host(v, "v", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want_host(start_pos, "start_pos", torch.int32, (B,))
+    if valid_len is not None:
+        _want_host(valid_len, "valid_len", torch.int32, (B,))
+    _want_host(out, "out", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _check(load().grok_prefill_pipe_submit(pipe, _ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), _ptr(valid_len),
+                                           _ptr(out)))
+
+
+def prefill_pipe_wait(pipe) -> int:
+    """Block until every queued step finished; returns the OR of their device status bits."""
+    st = ctypes.c_int32(0)
+    _check(load().grok_prefill_pipe_wait(pipe, ctypes.byref(st)))
+    return int(st.value)
+
+
+def prefill_pipe_destroy(pipe) -> None:
+    _check(load().grok_prefill_pipe_destroy(pipe))

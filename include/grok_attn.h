@@ -194,6 +194,45 @@ grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16
                                          const int32_t* kv_len, int B, int Tmax, grok_bf16* out,
                                          int32_t* dev_status, void* stream);
 
+/*
+ * Host-buffer prefill pipeline. The pages feed the attention core from a model
+ * on the same device and have no counterpart; this runtime object is for
+ * callers whose q, k, v arrive in host memory and whose output goes back there
+ * (a serving front end). A pipeline owns device double buffers and three CUDA
+ * streams (host-to-device copies, kernels, device-to-host copies), so the
+ * copies of one step overlap the kernels of the steps before and after it.
+ *
+ * grok_prefill_pipe_create: B, T, Tmax as for grok_rope_kv_append and
+ *   grok_attn_prefill. cache_k, cache_v are the caller's device caches
+ *   [B,Tmax,8,128] bf16 (16-byte aligned): every step appends to them and
+ *   attends over them, and they must stay allocated until destroy. Allocates
+ *   about B*T*(5*48 + 4*8)*128*2 bytes of device memory on the current device,
+ *   which the pipeline uses from then on. *pipe receives the handle.
+ * grok_prefill_pipe_submit: queue one step. Copy q [B,T,48,128], k and v
+ *   [B,T,8,128], start_pos [B] and valid_len [B] (NULL: every token valid) from
+ *   host memory; run grok_rope_kv_append then grok_attn_prefill; copy the output
+ *   [B,T,48,128] to host memory at out. Returns once the work is queued. The
+ *   host buffers must stay valid, the inputs unchanged and the output unread
+ *   until the next grok_prefill_pipe_wait. Page-locked host memory
+ *   (cudaHostAlloc, cudaHostRegister) lets the copies overlap; pageable memory
+ *   works but serialises them. Steps run in submission order. Argument errors
+ *   are returned before anything is queued.
+ * grok_prefill_pipe_wait: block until every queued step has finished.
+ *   *dev_status (nullable) receives the OR of the steps' device status words
+ *   (GROK_DEV_* bits, 0 when every sequence's integers were valid); the word is
+ *   then cleared.
+ * grok_prefill_pipe_destroy: wait, then free everything. NULL is ignored.
+ * One host thread at a time may use a pipeline.
+ */
+typedef struct grok_prefill_pipe grok_prefill_pipe;
+grok_status grok_prefill_pipe_create(int B, int T, int Tmax, grok_bf16* cache_k, grok_bf16* cache_v,
+                                     grok_prefill_pipe** pipe);
+grok_status grok_prefill_pipe_submit(grok_prefill_pipe* pipe, const grok_bf16* q, const grok_bf16* k,
+                                     const grok_bf16* v, const int32_t* start_pos, const int32_t* valid_len,
+                                     grok_bf16* out);
+grok_status grok_prefill_pipe_wait(grok_prefill_pipe* pipe, int32_t* dev_status);
+grok_status grok_prefill_pipe_destroy(grok_prefill_pipe* pipe);
+
 #ifdef __cplusplus
 }
 #endif
