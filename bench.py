@@ -41,8 +41,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
@@ -50,6 +50,13 @@ def parse_args():
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one workload only (profiling); implies --no-cpu-baseline --no-e2e")
     return ap.parse_args()
+
+
+def time_stats(ms_list) -> dict:
+    """Mean, median, min and 90th percentile of per-step kernel times (ms)."""
+    a = np.asarray(ms_list, dtype=np.float64)
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "min": float(a.min()),
+            "p90": float(np.percentile(a, 90))}
 
 
 # ----------------------------------------------------------------------------- work counts
@@ -311,8 +318,10 @@ def run_ours(args, rank: int, world: int, dist):
         dist.barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end) / args.steps
-    ms_append = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    ms_prefill = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    append_times = [e[0].elapsed_time(e[1]) for e in ev]
+    prefill_times = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_append = float(np.mean(append_times))
+    ms_prefill = float(np.mean(prefill_times))
     ms, ms_prefill, ms_append = max_over_ranks([ms, ms_prefill, ms_append], dist, dev)
     value = whole_job_rate(flops, world, ms, 1e12)
     prefill_tflops = flops / (ms_prefill * 1e-3) / 1e12
@@ -336,6 +345,7 @@ def run_ours(args, rank: int, world: int, dist):
                    "l2": "inputs larger than L2 (q, q_rot, out 100 MB each + caches 34 MB)",
                    "parallelism": f"replicas x{world} (independent sequences, no exchange)"},
         "kernels_ms": {"rope_kv_append": ms_append, "prefill": ms_prefill},
+        "kernels_ms_stats": {"rope_kv_append": time_stats(append_times), "prefill": time_stats(prefill_times)},
         "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": prefill_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": prefill_tflops / peak_tf, "peak_source": f"bf16_tflops ({peak_kind})",
                      "traffic": measured_traffic("prefill_kernel"), "traffic_unit": "bytes per launch (ncu)"},
@@ -463,9 +473,10 @@ def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
     b_.record(stream)
     torch.cuda.synchronize()
     ms_eager = a.elapsed_time(b_) / args.steps
-    ms_dec = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    ms_comb = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
-    ms_app = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    dec_times = [e[1].elapsed_time(e[2]) for e in ev]
+    comb_times = [e[2].elapsed_time(e[3]) for e in ev]
+    app_times = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_dec, ms_comb, ms_app = (float(np.mean(x)) for x in (dec_times, comb_times, app_times))
     # The step as a serving loop runs it: the K steps captured once in a CUDA graph
     # and replayed, so the three short launches per step cost no host round trips.
     side = torch.cuda.Stream()
@@ -496,6 +507,8 @@ def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
         "ms_per_step_eager": ms_eager,
         "algorithmic_bytes_per_step": nbytes,
         "kernels_ms": {"rope_kv_append": ms_app, "decode": ms_dec, "combine": ms_comb},
+        "kernels_ms_stats": {"rope_kv_append": time_stats(app_times), "decode": time_stats(dec_times),
+                             "combine": time_stats(comb_times)},
         "l2": f"{n_copies} rotating cache copies of {nbytes / 1e6:.0f} MB used rows each",
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": gbs_kernel, "peak": peak_bw,
                      "unit": "GB/s", "frac": gbs_kernel / peak_bw, "peak_source": f"hbm_gbs ({peak_kind})",
