@@ -1,0 +1,102 @@
+"""Pins of the oracle's Q/K/V projection: exact rational brute force, identity and
+one-hot weights (column layout), exact scaling, a library matmul, and the fused
+step's position-0 special case."""
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from oracle import bf16, projection as P, rope
+
+
+ONE = np.uint16(0x3F80)  # bf16 1.0
+
+
+def _rand_bf16(rng, shape, scale=1.0):
+    return bf16.from_f32((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def _nearest_bf16_of_fraction(v: Fraction) -> float:
+    """Brute force: the bf16 value nearest the exact rational (ties to the even pattern)."""
+    f = float(v)
+    base = int(np.float32(f).view(np.uint32) >> 16)
+    cands = []
+    for d in (-2, -1, 0, 1, 2):
+        b = (base + d) & 0xFFFF
+        val = float(bf16.to_f64(np.array([b], dtype=np.uint16))[0])
+        if np.isfinite(val):
+            cands.append((abs(Fraction(val) - v), b % 2, val))
+    cands.sort()
+    return cands[0][2]
+
+
+def test_linear_equals_exact_rational_brute_force():
+    rng = np.random.default_rng(20)
+    x = _rand_bf16(rng, (2, 3, 5))
+    w = _rand_bf16(rng, (5, 4))
+    got = bf16.to_f64(P.linear(x, w))
+    xf, wf = bf16.to_f64(x), bf16.to_f64(w)
+    for a in range(2):
+        for t in range(3):
+            for n in range(4):
+                exact = sum(Fraction(float(xf[a, t, i])) * Fraction(float(wf[i, n])) for i in range(5))
+                assert got[a, t, n] == _nearest_bf16_of_fraction(exact)
+
+
+def test_identity_weights_return_x_in_the_query_heads():
+    rng = np.random.default_rng(21)
+    x = _rand_bf16(rng, (1, 3, P.MODEL_SIZE), 3.0)
+    w = np.zeros((P.MODEL_SIZE, P.QKV_COLUMNS), dtype=np.uint16)
+    w[np.arange(P.MODEL_SIZE), np.arange(P.MODEL_SIZE)] = ONE
+    q, k, v = P.qkv_projection(x, w)
+    assert np.array_equal(q.reshape(1, 3, -1), x)  # query head h, feature d = input column h*128 + d
+    assert not k.any() and not v.any()
+
+
+def test_one_hot_columns_land_in_the_right_head_and_feature():
+    rng = np.random.default_rng(22)
+    x = _rand_bf16(rng, (1, 2, P.MODEL_SIZE))
+    cases = [(0, "q", 0, 0), (6143, "q", 47, 127), (130, "q", 1, 2), (6144, "k", 0, 0), (6144 + 3 * 128 + 5, "k", 3, 5),
+             (7168, "v", 0, 0), (8191, "v", 7, 127)]
+    for col, which, head, d in cases:
+        w = np.zeros((P.MODEL_SIZE, P.QKV_COLUMNS), dtype=np.uint16)
+        w[7, col] = ONE
+        out = dict(zip("qkv", P.qkv_projection(x, w)))
+        t = out[which]
+        assert np.array_equal(t[:, :, head, d], x[:, :, 7])
+        mask = np.ones(t.shape, dtype=bool)
+        mask[:, :, head, d] = False
+        assert not t[mask].any()
+        assert all(not out[o].any() for o in "qkv" if o != which)
+
+
+def test_scaling_by_a_power_of_two_is_exact():
+    rng = np.random.default_rng(23)
+    x = _rand_bf16(rng, (1, 4, 64))
+    w = _rand_bf16(rng, (64, 32))
+    x2 = bf16.from_f64(bf16.to_f64(x) * 4.0)
+    assert np.array_equal(bf16.to_f64(P.linear(x2, w)), bf16.to_f64(P.linear(x, w)) * 4.0)
+
+
+def test_linear_matches_torch_matmul_in_fp64():
+    rng = np.random.default_rng(24)
+    x = _rand_bf16(rng, (3, 7, 96))
+    w = _rand_bf16(rng, (96, 40))
+    ref = torch.from_numpy(bf16.to_f64(x)) @ torch.from_numpy(bf16.to_f64(w))
+    assert np.array_equal(P.linear(x, w), bf16.from_f64(ref.numpy()))
+
+
+def test_fused_step_at_position_zero_keeps_the_projection():
+    rng = np.random.default_rng(25)
+    x = _rand_bf16(rng, (1, 1, P.MODEL_SIZE))
+    w = _rand_bf16(rng, (P.MODEL_SIZE, P.QKV_COLUMNS), 3.0 / np.sqrt(P.MODEL_SIZE))
+    ck = _rand_bf16(rng, (1, 4, 8, 128))
+    cv = _rand_bf16(rng, (1, 4, 8, 128))
+    q, k, v = P.qkv_projection(x, w)
+    q_rot, nk, nv = P.qkv_rope_append(x, w, np.array([0]), ck, cv)
+    assert np.array_equal(q_rot, q)            # cos 0 = 1, sin 0 = 0
+    assert np.array_equal(nk[0, 0], k[0, 0]) and np.array_equal(nv[0, 0], v[0, 0])
+    assert np.array_equal(nk[0, 1:], ck[0, 1:])
+    # at another position the rotation is the RoPE oracle's
+    q_rot3, nk3, _ = P.qkv_rope_append(x, w, np.array([3]), ck, cv)
+    assert np.array_equal(q_rot3, rope.rotary_embedding(q, np.array([3])))
