@@ -42,6 +42,9 @@ EXPORTS = (
     "grok_prefill_pipe_submit",
     "grok_prefill_pipe_wait",
     "grok_prefill_pipe_destroy",
+    "grok_qkv_project",
+    "grok_qkv_workspace",
+    "grok_qkv_rope_append",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -90,6 +93,12 @@ def load() -> ctypes.CDLL:
     lib.grok_prefill_pipe_wait.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
     lib.grok_prefill_pipe_destroy.restype = I
     lib.grok_prefill_pipe_destroy.argtypes = [P]
+    lib.grok_qkv_project.restype = I
+    lib.grok_qkv_project.argtypes = [P, P, I, P, P, P]
+    lib.grok_qkv_workspace.restype = I
+    lib.grok_qkv_workspace.argtypes = [I, I, ctypes.POINTER(S)]
+    lib.grok_qkv_rope_append.restype = I
+    lib.grok_qkv_rope_append.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P, P]
     _lib = lib
     return lib
 
@@ -285,3 +294,43 @@ def prefill_pipe_wait(pipe) -> int:
 
 def prefill_pipe_destroy(pipe) -> None:
     _check(load().grok_prefill_pipe_destroy(pipe))
+
+
+MODEL_SIZE = 6144
+QKV_COLUMNS = (N_Q_HEADS + 2 * N_KV_HEADS) * HEAD_DIM
+
+
+def qkv_project(x, w, y, dev_status=None, stream=None) -> None:
+    """y [M, 8192] = x [M, 6144] . w [6144, 8192] (bf16, fp32 accumulation)."""
+    M = x.shape[0]
+    _want(x, "x", torch.bfloat16, (M, MODEL_SIZE))
+    _want(w, "w", torch.bfloat16, (MODEL_SIZE, QKV_COLUMNS))
+    _want(y, "y", torch.bfloat16, (M, QKV_COLUMNS))
+    _check(load().grok_qkv_project(_ptr(x), _ptr(w), M, _ptr(y), _ptr(dev_status), _stream(stream)))
+
+
+def qkv_workspace(B: int, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().grok_qkv_workspace(int(B), int(T), ctypes.byref(n)))
+    return int(n.value)
+
+
+def alloc_qkv_workspace(B: int, T: int, device=None) -> torch.Tensor:
+    return torch.empty(qkv_workspace(B, T), dtype=torch.uint8, device=device or "cuda")
+
+
+def qkv_rope_append(x, w, start_pos, q_rot, cache_k, cache_v, workspace, dev_status=None, stream=None) -> None:
+    """Projection fused with RoPE and the cache append (see grok_qkv_rope_append)."""
+    B, T = x.shape[0], x.shape[1]
+    Tmax = cache_k.shape[1]
+    _want(x, "x", torch.bfloat16, (B, T, MODEL_SIZE))
+    _want(w, "w", torch.bfloat16, (MODEL_SIZE, QKV_COLUMNS))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_qkv_rope_append(_ptr(x), _ptr(w), _ptr(start_pos), B, T, Tmax, _ptr(q_rot), _ptr(cache_k),
+                                       _ptr(cache_v), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                       _stream(stream)))

@@ -1,0 +1,412 @@
+// Q/K/V projection on the 5th-generation tensor cores, optionally fused with
+// RoPE and the KV-cache append.
+//
+// Grok-1 code-reading guide, ch. 4 "model.py close reading I": §4.1 Linear
+// (weight [input_size, output_size], out = dot(x, w) in the input dtype),
+// §4.5.1 Q/K/V projection (three bias-free Linears, 6144 -> 48 x 128, 8 x 128,
+// 8 x 128, reshaped head-major), §4.3.1 RotaryEmbedding and §4.4 (rotate Q and
+// K at offset = step, write rotated K and raw V into the cache at step).
+//
+// One GEMM: Y [M, 8192] = X [M, 6144] . W [6144, 8192], W = [W_q | W_k | W_v]
+// side by side, M = B * T rows (b * T + i). bf16 operands, fp32 accumulation
+// in TMEM, one rounding to bf16 per output. Output column h*128 + d is query
+// head h, 6144 + g*128 + d key head g, 7168 + g*128 + d value head g.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: per 64-wide K block one X box [128 rows x 64] and
+//               four W boxes [64 rows x 64 columns] into a 4-stage ring
+//   warp 1      TMEM owner and MMA issuer (converged; one fixed lane issues)
+//   warps 2-5   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
+//               row per thread
+// Tile = 128 rows x 256 columns (two heads); tcgen05.mma M=128, N=256, K=16,
+// A = X (K-major), B = W (N-contiguous rows, MN-major), both 128-byte
+// swizzled. Two 256-column TMEM accumulators: the epilogue of one tile
+// overlaps the products of the next. Tiles go in groups of eight 128-row
+// blocks by all 32 column blocks, so the tiles in flight share X and W in L2.
+//
+// Epilogues: plain (write Y) or fused (q heads: RoPE -> q_rot; k heads: RoPE
+// -> cache_k at row start_pos[b] + i; v heads -> cache_v). The rotation is the
+// one of rope_kv_append (separately rounded fp32 products and sum of the bf16
+// value and the fp32 cos / sin) with cos / sin taken from a per-step table
+// that qkv_table_kernel fills with the shared fp64 routine.
+#include "common.cuh"
+#include "host.cuh"
+#include "rope_math.cuh"
+
+namespace grok {
+
+constexpr int kQkvK = 6144;                 // model size
+constexpr int kQkvN = 8192;                 // 48 * 128 + 2 * 8 * 128
+constexpr int kQkvBM = 128, kQkvBN = 256, kQkvBK = 64;
+constexpr int kQkvStages = 4;
+constexpr int kQkvThreads = 192;
+constexpr int kQkvGroupM = 8;
+constexpr int kQkvKBlocks = kQkvK / kQkvBK;                 // 96
+constexpr int kQkvNTiles = kQkvN / kQkvBN;                  // 32
+constexpr int kQkvABytes = kQkvBM * kQkvBK * 2;             // 16 KB
+constexpr int kQkvBBox = kQkvBK * 64 * 2;                   // 8 KB: 64 K rows x 64 columns
+constexpr int kQkvBBytes = 4 * kQkvBBox;                    // 32 KB
+constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;     // 48 KB
+
+struct QkvBars {
+  uint64_t full[kQkvStages], empty[kQkvStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kQkvSmem = kQkvStages * kQkvStageBytes + int(sizeof(QkvBars)) + 1024;
+
+struct QkvParams {
+  int M, T, Tmax, n_mtiles, n_tiles;
+  const int32_t* start_pos;     // fused epilogue only
+  const float* cos_tab;         // [M][64]
+  const float* sin_tab;
+  uint4* y;                     // plain: [M][8192]
+  uint4* q_rot;                 // fused: [B][T][48][128]
+  uint4* cache_k;               // fused: [B][Tmax][8][128]
+  uint4* cache_v;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void qkv_tile(const QkvParams& p, int t, int& m, int& n) {
+  const int per_group = kQkvGroupM * kQkvNTiles;
+  const int g = t / per_group, r = t % per_group;
+  const int gm = min(kQkvGroupM, p.n_mtiles - g * kQkvGroupM);
+  m = g * kQkvGroupM + r % gm;
+  n = r / gm;
+}
+
+// cos / sin of every row's position for the fused epilogue (row = b * T + i,
+// position start_pos[b] + i); rows of an invalid sequence are left unset.
+__global__ void qkv_table_kernel(const int32_t* __restrict__ start_pos, int M, int T, int Tmax,
+                                 float* __restrict__ cos_tab, float* __restrict__ sin_tab, int32_t* status) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)M * 64) return;
+  const int row = int(idx >> 6), j = int(idx & 63);
+  const int b = row / T, i = row % T;
+  const int s = __ldg(start_pos + b);
+  if (s < 0 || (long long)s + T > Tmax) {
+    if (i == 0 && j == 0) report(status, GROK_DEV_BAD_START);
+    return;
+  }
+  float c, sn;
+  rope_cos_sin(__fmul_rn(float(s + i), rope_inv_freq(j)), c, sn);
+  cos_tab[idx] = c;
+  sin_tab[idx] = sn;
+}
+
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// 32 accumulator columns -> 16 packed bf16 pairs (round to nearest even).
+__device__ __forceinline__ void qkv_round32(const uint32_t (&a)[32], uint32_t (&o)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+}
+
+// RoPE on one row's features d0 .. d0+31 (x1, packed bf16) and d0+64 .. d0+95
+// (x2): x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin, every product and sum
+// rounded to fp32 separately, then to bf16.
+__device__ __forceinline__ void qkv_rotate32(uint32_t (&x1)[16], uint32_t (&x2)[16], const float* cs,
+                                             const float* sn) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float a0 = bf16lo_to_f32(x1[e]), a1 = bf16hi_to_f32(x1[e]);
+    const float b0 = bf16lo_to_f32(x2[e]), b1 = bf16hi_to_f32(x2[e]);
+    const float c0 = cs[2 * e], c1 = cs[2 * e + 1], s0 = sn[2 * e], s1 = sn[2 * e + 1];
+    const float y1a = __fadd_rn(__fmul_rn(a0, c0), -__fmul_rn(b0, s0));
+    const float y1b = __fadd_rn(__fmul_rn(a1, c1), -__fmul_rn(b1, s1));
+    const float y2a = __fadd_rn(__fmul_rn(b0, c0), __fmul_rn(a0, s0));
+    const float y2b = __fadd_rn(__fmul_rn(b1, c1), __fmul_rn(a1, s1));
+    x1[e] = pack_bf16x2(y1a, y1b);
+    x2[e] = pack_bf16x2(y2a, y2b);
+  }
+}
+
+template <bool kFused>
+__global__ void __launch_bounds__(kQkvThreads, 1)
+    qkv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const QkvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvStages * kQkvStageBytes);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQkvStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->acc_full[s], 1);
+      mbar_init(&bars->acc_empty[s], 128);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+        int m, n;
+        qkv_tile(p, t, m, n);
+        for (int kb = 0; kb < kQkvKBlocks; ++kb, ++it) {
+          const int st = it % kQkvStages;
+          if (!mbar_wait(&bars->empty[st], ((it / kQkvStages) & 1) ^ 1, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + st * kQkvStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
+          tma_load_4d(sa, &tm_x, &bars->full[st], kb * kQkvBK, m * kQkvBM, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tma_load_4d(sa + kQkvABytes + c * kQkvBBox, &tm_w, &bars->full[st], n * kQkvBN + c * 64, kb * kQkvBK, 0, 0);
+        }
+      }
+      // Drain: copies still in flight (only after an abort) land before the CTA exits.
+      volatile int never = 0;
+      for (int u = max(0, it - kQkvStages); u < it; ++u)
+        mbar_wait(&bars->full[u % kQkvStages], (u / kQkvStages) & 1, &never, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = make_idesc_bf16(kQkvBM, kQkvBN, 1);
+    int it = 0, tc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tc) {
+      const int ab = tc & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[ab], ((tc >> 1) & 1) ^ 1, abort, p.status))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + ab * kQkvBN;
+      for (int kb = 0; kb < kQkvKBlocks; ++kb, ++it) {
+        const int st = it % kQkvStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[st], (it / kQkvStages) & 1, abort, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (leader) {
+          const uint32_t sa = smem_u32(smem + st * kQkvStageBytes);
+          const uint64_t adesc = make_sdesc_sw128(sa, 16, 1024);
+          const uint64_t bdesc = make_sdesc_sw128(sa + kQkvABytes, kQkvBBox, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 64 in steps of 16: A +32 B, B +16 rows (2048 B)
+            umma_ss(d, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
+                    (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bars->empty[st]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) umma_commit(&bars->acc_full[ab]);
+      __syncwarp();
+    }
+    // No MMA may still be running when TMEM is released.
+    if (leader) umma_commit(&bars->mma_done);
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(&bars->mma_done, 0, &never, p.status);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t tlane = uint32_t(quad * 32) << 16;
+    int tc = 0;
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tc) {
+      int m, n;
+      qkv_tile(p, t, m, n);
+      const int ab = tc & 1;
+      const bool ok = mbar_wait(&bars->acc_full[ab], (tc >> 1) & 1, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + tlane + ab * kQkvBN;
+      const int row = m * kQkvBM + r;
+      const bool live = row < p.M;
+      if (!kFused) {
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * kQkvN + n * kQkvBN) * 2;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t a[32], o[16];
+          tmem_ld32(acc + c * 32, a);
+          tmem_wait_ld_dep(a);
+          qkv_round32(a, o);
+          if (live) {
+            st_global_v8(dst + c * 64, o);
+            st_global_v8(dst + c * 64 + 32, o + 8);
+          }
+        }
+      } else {
+        const int b = row / p.T, i = row % p.T;
+        const int s = live ? __ldg(p.start_pos + b) : 0;
+        const bool write = live && s >= 0 && (long long)s + p.T <= p.Tmax;
+        const bool rotate = n < (kQHeads + kKVHeads) * kD / kQkvBN;     // query and key columns
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {   // the tile's two heads
+          const int col = n * kQkvBN + hh * kD;   // first output column of the head
+          uint8_t* dst;
+          if (col < kQHeads * kD) {
+            dst = reinterpret_cast<uint8_t*>(p.q_rot) + ((size_t)row * kQHeads * kD + col) * 2;
+          } else if (col < (kQHeads + kKVHeads) * kD) {
+            const int g = (col - kQHeads * kD) / kD;
+            dst = reinterpret_cast<uint8_t*>(p.cache_k) + ((((size_t)b * p.Tmax + s + i) * kKVHeads + g) * kD) * 2;
+          } else {
+            const int g = (col - (kQHeads + kKVHeads) * kD) / kD;
+            dst = reinterpret_cast<uint8_t*>(p.cache_v) + ((((size_t)b * p.Tmax + s + i) * kKVHeads + g) * kD) * 2;
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {   // features 32c .. 32c+31 paired with 64+32c ..
+            uint32_t a[32], x1[16], x2[16];
+            tmem_ld32(acc + hh * kD + c * 32, a);
+            tmem_wait_ld_dep(a);
+            qkv_round32(a, x1);
+            tmem_ld32(acc + hh * kD + 64 + c * 32, a);
+            tmem_wait_ld_dep(a);
+            qkv_round32(a, x2);
+            if (rotate && write) {
+              float cs[32], sn[32];
+              const float4* cp = reinterpret_cast<const float4*>(p.cos_tab + (size_t)row * 64 + c * 32);
+              const float4* sp = reinterpret_cast<const float4*>(p.sin_tab + (size_t)row * 64 + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 cv = __ldg(cp + q), sv = __ldg(sp + q);
+                cs[4 * q] = cv.x, cs[4 * q + 1] = cv.y, cs[4 * q + 2] = cv.z, cs[4 * q + 3] = cv.w;
+                sn[4 * q] = sv.x, sn[4 * q + 1] = sv.y, sn[4 * q + 2] = sv.z, sn[4 * q + 3] = sv.w;
+              }
+              qkv_rotate32(x1, x2, cs, sn);
+            }
+            if (write) {
+              st_global_v8(dst + c * 64, x1);
+              st_global_v8(dst + c * 64 + 32, x1 + 8);
+              st_global_v8(dst + 128 + c * 64, x2);
+              st_global_v8(dst + 128 + c * 64 + 32, x2 + 8);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty[ab]);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, QkvParams& prm, void* stream) {
+  int sms = 0;
+  grok_status st = device_sm_count(&sms);
+  if (st != GROK_OK) return st;
+  CUtensorMap tx, tw;
+  {
+    const uint64_t dims[4] = {uint64_t(kQkvK), uint64_t(M), 1, 1};
+    const uint64_t strides[3] = {uint64_t(kQkvK) * 2, uint64_t(kQkvK) * 2 * M, uint64_t(kQkvK) * 2 * M};
+    const uint32_t box[4] = {uint32_t(kQkvBK), uint32_t(kQkvBM), 1, 1};
+    if ((st = encode_tmap_bf16_4d(&tx, x, dims, strides, box)) != GROK_OK) return st;
+  }
+  {
+    const uint64_t dims[4] = {uint64_t(kQkvN), uint64_t(kQkvK), 1, 1};
+    const uint64_t strides[3] = {uint64_t(kQkvN) * 2, uint64_t(kQkvN) * 2 * kQkvK, uint64_t(kQkvN) * 2 * kQkvK};
+    const uint32_t box[4] = {64, uint32_t(kQkvBK), 1, 1};
+    if ((st = encode_tmap_bf16_4d(&tw, w, dims, strides, box)) != GROK_OK) return st;
+  }
+  prm.M = M;
+  prm.n_mtiles = (M + kQkvBM - 1) / kQkvBM;
+  prm.n_tiles = prm.n_mtiles * kQkvNTiles;
+  const int grid = prm.n_tiles < sms ? prm.n_tiles : sms;
+  auto kernel = fused ? qkv_kernel<true> : qkv_kernel<false>;
+  static bool attr_set[2] = {false, false};  // idempotent: every thread would set the same value
+  if (!attr_set[fused]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem);
+    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    attr_set[fused] = true;
+  }
+  kernel<<<grid, kQkvThreads, kQkvSmem, static_cast<cudaStream_t>(stream)>>>(tx, tw, prm);
+  return check_launch("qkv");
+}
+
+}  // namespace grok
+
+using namespace grok;
+
+extern "C" grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y,
+                                        int32_t* dev_status, void* stream) {
+  if (!x || !w || !y) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: null pointer");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y))
+    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: tensors must be 16-byte aligned");
+  if (M < 1) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: need M >= 1 (M=%d)", M);
+  QkvParams prm = {};
+  prm.T = 1;
+  prm.Tmax = 1;
+  prm.y = reinterpret_cast<uint4*>(y);
+  prm.status = dev_status;
+  return qkv_launch(false, x, w, M, prm, stream);
+}
+
+extern "C" grok_status grok_qkv_workspace(int B, int T, size_t* bytes) {
+  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_workspace: null pointer");
+  if (B < 1 || T < 1) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_workspace: need B, T >= 1");
+  *bytes = size_t(B) * T * 64 * 2 * sizeof(float);
+  return GROK_OK;
+}
+
+extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
+                                            int T, int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v,
+                                            void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!x || !w || !start_pos || !q_rot || !cache_k || !cache_v || !workspace)
+    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: null pointer");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) ||
+      !aligned16(workspace))
+    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: tensors must be 16-byte aligned");
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+                GROK_MAX_POSITION, B, T, Tmax);
+  size_t need = 0;
+  grok_qkv_workspace(B, T, &need);
+  if (ws_bytes < need)
+    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: workspace of %zu bytes, need %zu", ws_bytes, need);
+  const long long M = (long long)B * T;
+  if (M > (1LL << 30)) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: B * T too large");
+  QkvParams prm = {};
+  prm.T = T;
+  prm.Tmax = Tmax;
+  prm.start_pos = start_pos;
+  prm.cos_tab = static_cast<const float*>(workspace);
+  prm.sin_tab = prm.cos_tab + M * 64;
+  prm.q_rot = reinterpret_cast<uint4*>(q_rot);
+  prm.cache_k = reinterpret_cast<uint4*>(cache_k);
+  prm.cache_v = reinterpret_cast<uint4*>(cache_v);
+  prm.status = dev_status;
+  const long long total = M * 64;
+  qkv_table_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      start_pos, int(M), T, Tmax, const_cast<float*>(prm.cos_tab), const_cast<float*>(prm.sin_tab), dev_status);
+  grok_status st = check_launch("qkv table");
+  if (st != GROK_OK) return st;
+  return qkv_launch(true, x, w, int(M), prm, stream);
+}

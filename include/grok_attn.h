@@ -195,6 +195,33 @@ grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16
                                          int32_t* dev_status, void* stream);
 
 /*
+ * Q/K/V projection (code-reading guide ch. 4 §4.1 Linear, §4.5.1 Q/K/V
+ * projection): the three bias-free Linears of the attention call as one
+ * product with the weights side by side.
+ *   x [M, 6144] bf16 (M = B*T rows, row b*T + i), w [6144, 8192] bf16 in the
+ *   pages' [input, output] layout: columns h*128 + d are query head h,
+ *   6144 + g*128 + d key head g, 7168 + g*128 + d value head g.
+ * fp32 accumulation on the tensor cores, one rounding to bf16 per output.
+ *
+ * grok_qkv_project: y [M, 8192] = x . w. dev_status is unused (nullable).
+ * grok_qkv_rope_append: the projection fused with grok_rope_kv_append. q heads
+ *   are rotated into q_rot [B,T,48,128]; k heads are rotated and v heads copied
+ *   into rows [start_pos[b], start_pos[b]+T) of cache_k / cache_v
+ *   [B,Tmax,8,128]. Bits equal grok_rope_kv_append applied to the bf16
+ *   projection. workspace: caller-owned device memory of at least
+ *   grok_qkv_workspace(B, T) bytes (a per-step cos/sin table), 16-byte aligned.
+ *   A sequence whose start_pos[b] + T > Tmax (or start < 0) sets
+ *   GROK_DEV_BAD_START and none of its rows are written.
+ * All pointers device-resident, 16-byte aligned; work is asynchronous on stream.
+ */
+grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y, int32_t* dev_status,
+                             void* stream);
+grok_status grok_qkv_workspace(int B, int T, size_t* bytes);
+grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B, int T,
+                                 int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * Host-buffer prefill pipeline. The pages feed the attention core from a model
  * on the same device and have no counterpart; this runtime object is for
  * callers whose q, k, v arrive in host memory and whose output goes back there

@@ -41,12 +41,16 @@ HEAD_DIM = 128
 QKV_COLUMNS = (N_Q_HEADS + 2 * N_KV_HEADS) * HEAD_DIM  # 8192
 
 
-def linear(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
-    """§4.1 Linear without bias: bf16 x [..., K] times bf16 w [K, N], exact sum rounded to bf16."""
+def linear_exact(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """The sum of §4.1's dot before its rounding to bf16, in fp64: x [..., K] . w [K, N]."""
     lead = x_bits.shape[:-1]
     x = bf16.to_f64(x_bits).reshape(-1, x_bits.shape[-1])
-    w = bf16.to_f64(w_bits)
-    return bf16.from_f64(x @ w).reshape(*lead, w_bits.shape[1])
+    return (x @ bf16.to_f64(w_bits)).reshape(*lead, w_bits.shape[1])
+
+
+def linear(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """§4.1 Linear without bias: bf16 x [..., K] times bf16 w [K, N], exact sum rounded to bf16."""
+    return bf16.from_f64(linear_exact(x_bits, w_bits))
 
 
 def qkv_projection(x_bits: np.ndarray, w_bits: np.ndarray):

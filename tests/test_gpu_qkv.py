@@ -1,0 +1,130 @@
+"""Q/K/V projection parity: the tensor-core GEMM against the fp64 oracle, and the
+fused projection + RoPE + cache append against the oracle's RoPE applied to the
+kernel's own projection (bit for bit)."""
+import numpy as np
+import pytest
+import torch
+
+import grok_gqa_attention_gb300 as G
+import workloads as W
+from oracle import bf16, projection as P, rope
+
+pytestmark = pytest.mark.gpu
+
+
+# The tensor cores accumulate the 6144-term dot in fp32: 384 additions of a
+# 16-term chunk into the accumulator, each rounding to half an fp32 ulp of a
+# partial sum. With |x| and |w| as generated, partial sums stay below 16, so
+# the accumulated error is at most 384 * 2^-20 = 3.7e-4 (typically ~1e-5).
+ACC_BOUND = 384 * 2.0 ** -20
+
+
+def _projection_check(got_bits, exact, what, max_mismatch_frac=0.01):
+    """Within half a bf16 ulp of the exact sum plus the fp32 accumulation bound;
+    equal to the oracle's rounded bits for all but a small fraction."""
+    g = bf16.to_f64(got_bits)
+    assert np.all(np.isfinite(g))
+    mag = np.maximum(np.abs(exact), np.abs(g)).astype(np.float32)
+    half_ulp = np.spacing(mag).astype(np.float64) * 2 ** 15
+    err = np.abs(g - exact)
+    assert np.all(err <= half_ulp + ACC_BOUND), f"{what}: worst excess {float((err - half_ulp).max())}"
+    frac = float(np.mean(got_bits != bf16.from_f64(exact)))
+    assert frac <= max_mismatch_frac, f"{what}: {frac:.4%} of outputs differ from the rounded exact sum"
+    return frac
+
+
+@pytest.fixture(scope="module")
+def small():
+    return W.projection(B=2, T=200, Tmax=512, start_pos=[100, 37], seed=50)
+
+
+def test_projection_matches_exact_oracle(small):
+    x2d = small.x.reshape(-1, P.MODEL_SIZE)
+    w = small.w.cuda()
+    y = torch.empty((x2d.shape[0], P.QKV_COLUMNS), dtype=torch.bfloat16, device="cuda")
+    G.qkv_project(x2d.cuda(), w, y)
+    torch.cuda.synchronize()
+    got = W.bits(y.cpu())
+    _projection_check(got, P.linear_exact(W.bits(x2d), W.bits(small.w)), "projection M=400")
+
+
+def test_fused_equals_rope_append_of_own_projection(small):
+    B, T = small.x.shape[0], small.x.shape[1]
+    Tmax = small.cache_k.shape[1]
+    x, w = small.x.cuda(), small.w.cuda()
+    y = torch.empty((B * T, P.QKV_COLUMNS), dtype=torch.bfloat16, device="cuda")
+    G.qkv_project(x.reshape(B * T, -1), w, y)
+    ck, cv = small.cache_k.cuda(), small.cache_v.cuda()
+    q_rot = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = G.alloc_qkv_workspace(B, T)
+    G.qkv_rope_append(x, w, small.start_pos.cuda(), q_rot, ck, cv, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = W.bits(y.cpu()).reshape(B, T, -1)
+    q = yb[..., :6144].reshape(B, T, 48, 128)
+    k = yb[..., 6144:7168].reshape(B, T, 8, 128)
+    v = yb[..., 7168:].reshape(B, T, 8, 128)
+    rq, rk, rv = rope.rope_kv_append(q, k, v, small.start_pos.numpy(), W.bits(small.cache_k), W.bits(small.cache_v))
+    assert np.array_equal(W.bits(q_rot.cpu()), rq)
+    assert np.array_equal(W.bits(ck.cpu()), rk)   # includes rows outside [start, start+T): untouched
+    assert np.array_equal(W.bits(cv.cpu()), rv)
+
+
+def test_fused_full_size_sampled_rows():
+    B, T, Tmax = 1, 8192, 8192
+    inp = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[0], seed=51)
+    x, w = inp.x.cuda(), inp.w.cuda()
+    y = torch.empty((B * T, P.QKV_COLUMNS), dtype=torch.bfloat16, device="cuda")
+    G.qkv_project(x.reshape(B * T, -1), w, y)
+    ck, cv = inp.cache_k.cuda(), inp.cache_v.cuda()
+    q_rot = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.qkv_rope_append(x, w, inp.start_pos.cuda(), q_rot, ck, cv, G.alloc_qkv_workspace(B, T), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(52)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 8191], rng.integers(0, T, 58)]))
+    yb = W.bits(y.cpu())[rows]
+    # the projection against the exact oracle on the sampled rows
+    _projection_check(yb, P.linear_exact(W.bits(inp.x)[0, rows], W.bits(inp.w)), "projection M=8192 (sampled rows)")
+    # the fused outputs against the oracle's RoPE of the kernel's projection, row by row
+    qb, kb = W.bits(q_rot.cpu())[0], W.bits(ck.cpu())[0]
+    vb = W.bits(cv.cpu())[0]
+    for n, i in enumerate(rows):
+        q = yb[n, :6144].reshape(1, 1, 48, 128)
+        k = yb[n, 6144:7168].reshape(1, 1, 8, 128)
+        assert np.array_equal(qb[i], rope.rotary_embedding(q, np.array([i]))[0, 0])
+        assert np.array_equal(kb[i], rope.rotary_embedding(k, np.array([i]))[0, 0])
+        assert np.array_equal(vb[i], yb[n, 7168:].reshape(8, 128))
+
+
+def test_bad_start_sets_status_and_writes_nothing_for_that_sequence():
+    B, T, Tmax = 2, 64, 128
+    inp = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[10, Tmax - T + 1], seed=53)
+    ck, cv = inp.cache_k.cuda(), inp.cache_v.cuda()
+    q_rot = torch.zeros((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.qkv_rope_append(inp.x.cuda(), inp.w.cuda(), inp.start_pos.cuda(), q_rot, ck, cv,
+                      G.alloc_qkv_workspace(B, T), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & G.DEV_BAD_START
+    assert np.array_equal(W.bits(ck.cpu())[1], W.bits(inp.cache_k)[1])
+    assert np.array_equal(W.bits(cv.cpu())[1], W.bits(inp.cache_v)[1])
+    assert not W.bits(q_rot.cpu())[1].any()
+    assert W.bits(q_rot.cpu())[0].any()             # the valid sequence was written
+
+
+def test_argument_checks():
+    B, T = 1, 8
+    x = torch.zeros((B, T, P.MODEL_SIZE), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((P.MODEL_SIZE, P.QKV_COLUMNS), dtype=torch.bfloat16, device="cuda")
+    ck = torch.zeros((B, 16, 8, 128), dtype=torch.bfloat16, device="cuda")
+    cv = torch.zeros_like(ck)
+    q_rot = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    start = torch.zeros(B, dtype=torch.int32, device="cuda")
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(G.GrokError):
+        G.qkv_rope_append(x, w, start, q_rot, ck, cv, small_ws)
+    assert G.load().grok_qkv_project(None, None, 4, None, None, None) == 1
+    assert G.qkv_workspace(B, T) == B * T * 64 * 2 * 4

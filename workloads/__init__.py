@@ -14,6 +14,12 @@ each rounded to bf16 (round to nearest even), then the per-sequence integers
 row at or after ``start_pos[b]`` is then overwritten with junk (alternating
 +-1e4, or NaN for a poison run): rows ``[start, start+T)`` must be written by the
 append and rows beyond must never be read.
+
+Projection inputs (``projection``): the same generator draws x [B,T,6144] as
+``randn`` (std 1) and the side-by-side Q/K/V weights w [6144, 8192] as
+``randn * 3 / sqrt(6144)`` (so projected q, k, v have std about 3, like the
+attention inputs above), both rounded to bf16, then cache_k, cache_v and the
+start positions as above.
 """
 from __future__ import annotations
 
@@ -175,3 +181,31 @@ def from_bits(a: np.ndarray) -> torch.Tensor:
     """A bf16 tensor whose storage is the given uint16 array."""
     a = np.ascontiguousarray(a, dtype=np.uint16)
     return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+
+
+MODEL_SIZE = 6144
+QKV_COLUMNS = (N_Q_HEADS + 2 * N_KV_HEADS) * HEAD_DIM
+
+
+@dataclasses.dataclass
+class ProjectionInputs:
+    """Host tensors for the Q/K/V projection: bf16 x, w, caches; int32 start positions."""
+
+    x: torch.Tensor          # [B, T, 6144]
+    w: torch.Tensor          # [6144, 8192]
+    cache_k: torch.Tensor    # [B, Tmax, 8, 128]
+    cache_v: torch.Tensor    # [B, Tmax, 8, 128]
+    start_pos: torch.Tensor  # [B] int32
+
+
+def projection(B: int, T: int, Tmax: int, start_pos, seed: int = 0, junk: str = "finite") -> ProjectionInputs:
+    """Seeded projection inputs (recipe in the module docstring)."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _randn_bf16(gen, (B, T, MODEL_SIZE), 1.0)
+    w = _randn_bf16(gen, (MODEL_SIZE, QKV_COLUMNS), 3.0 / float(np.sqrt(MODEL_SIZE)))
+    cache_k = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), 3.0)
+    cache_v = _randn_bf16(gen, (B, Tmax, N_KV_HEADS, HEAD_DIM), 3.0)
+    start = torch.as_tensor(np.asarray(start_pos, dtype=np.int32))
+    junk_rows_(cache_k, start, junk)
+    junk_rows_(cache_v, start, junk)
+    return ProjectionInputs(x, w, cache_k, cache_v, start)
