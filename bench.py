@@ -47,7 +47,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--no-qkv", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode", "qkv"], default=None,
                     help="run one workload only (profiling); implies --no-cpu-baseline --no-e2e")
     return ap.parse_args()
 
@@ -91,6 +92,7 @@ def source_digest(*paths: str) -> str:
 
 
 KERNEL_SOURCES = {
+    "qkv_kernel": ("grok_gqa_attention_gb300/csrc/qkv.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
     "prefill_kernel": ("grok_gqa_attention_gb300/csrc/prefill.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
     "decode_kernel": ("grok_gqa_attention_gb300/csrc/decode.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
 }
@@ -418,10 +420,83 @@ def run_ours(args, rank: int, world: int, dist):
     del q, k, v, ck, cv, q_rot, out
     torch.cuda.empty_cache()
 
+    # ---------------- Q/K/V projection (the step in front of the attention call)
+    if not args.no_qkv:
+        result["qkv_projection"] = run_qkv(args, rank, world, dist, dev, peaks, peak_kind)
+
     # ---------------- decode workload
     if not args.no_decode:
         result["decode"] = run_decode(args, rank, world, dist, dev, peaks, peak_kind)
     return result
+
+
+QKV_WORKLOAD = (1, 8192)  # B, T of the projection line: the prefill workload's tokens
+
+
+def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
+    """x [B,T,6144] . W [6144,8192] on tcgen05: plain (one launch) and fused with RoPE + append."""
+    import torch
+    import grok_gqa_attention_gb300 as G
+    import workloads as W
+    B, T = QKV_WORKLOAD
+    Tmax = T
+    inp = W.projection(B, T, Tmax, [0] * B, seed=rank)
+    x, w = inp.x.to(dev), inp.w.to(dev)
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    M = B * T
+    y = torch.empty((M, G.QKV_COLUMNS), dtype=torch.bfloat16, device=dev)
+    q_rot = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device=dev)
+    ws = G.alloc_qkv_workspace(B, T, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flops = 2.0 * M * G.MODEL_SIZE * G.QKV_COLUMNS
+    stream = torch.cuda.current_stream()
+    x2d = x.view(M, G.MODEL_SIZE)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e in evs:
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        t = [a.elapsed_time(b) for a, b in evs]
+        (m,) = max_over_ranks([float(np.mean(t))], dist, dev)
+        return m, t
+
+    ms_plain, t_plain = timed(lambda: G.qkv_project(x2d, w, y))
+    ms_fused, t_fused = timed(lambda: G.qkv_rope_append(x, w, start, q_rot, ck, cv, ws, status))
+    ms_cublas, _ = timed(lambda: torch.matmul(x2d, w))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the projection")
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tf_plain = flops / (ms_plain * 1e-3) / 1e12
+    out = {
+        "workload": f"qkv_b{B}_t{T}", "shape": {"M": M, "K": G.MODEL_SIZE, "N": G.QKV_COLUMNS},
+        "metric": "Q/K/V projection TFLOP/s (2*M*K*N per step)",
+        "value": whole_job_rate(flops, world, ms_fused, 1e12), "unit": "TFLOP/s", "ms_per_step": ms_fused,
+        "step": "grok_qkv_rope_append: cos/sin table kernel + projection GEMM with RoPE and cache-append epilogue",
+        "plain": {"ms": ms_plain, "TFLOP/s": tf_plain, "stats": time_stats(t_plain)},
+        "fused_stats": time_stats(t_fused),
+        "roofline": {"bound": "tensor", "kernel": "qkv_kernel (plain epilogue, one launch)", "achieved": tf_plain,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_plain / peak_tf,
+                     "peak_source": f"bf16_tflops ({peak_kind})", "traffic": measured_traffic("qkv_kernel"),
+                     "traffic_unit": "bytes per launch (ncu)"},
+        "cublas_context": {"op": "torch.matmul on the same bf16 product", "ms": ms_cublas,
+                           "TFLOP/s": flops / (ms_cublas * 1e-3) / 1e12},
+        "data": "synthetic (seeded randn -> bf16; weights randn*3/sqrt(6144))",
+        "l2": "inputs larger than L2 (x 100 MB, W 100 MB, y 134 MB)",
+        "gpu_launches": 3 * args.steps,
+    }
+    del x, w, ck, cv, y, q_rot
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_decode(args, rank, world, dist, dev, peaks, peak_kind):
@@ -550,7 +625,8 @@ def main():
     if args.only:
         args.no_cpu_baseline = True
         args.no_e2e = True
-        args.no_decode = args.only == "prefill"
+        args.no_decode = args.only != "decode"
+        args.no_qkv = args.only != "qkv"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -28,7 +28,9 @@
 // -> cache_k at row start_pos[b] + i; v heads -> cache_v). The rotation is the
 // one of rope_kv_append (separately rounded fp32 products and sum of the bf16
 // value and the fp32 cos / sin) with cos / sin taken from a per-step table
-// that qkv_table_kernel fills with the shared fp64 routine.
+// that qkv_table_kernel fills with the shared fp64 routine. The projection is
+// that kernel's programmatic dependent launch: its main loop runs while the
+// table is computed, and its epilogue waits for the table grid.
 #include "common.cuh"
 #include "host.cuh"
 #include "rope_math.cuh"
@@ -78,22 +80,35 @@ __device__ __forceinline__ void qkv_tile(const QkvParams& p, int t, int& m, int&
 }
 
 // cos / sin of every row's position for the fused epilogue (row = b * T + i,
-// position start_pos[b] + i); rows of an invalid sequence are left unset.
+// position start_pos[b] + i); rows of an invalid sequence are left unset. Each
+// thread evaluates kQkvTabPer frequencies of one row, independent fp64 chains
+// that keep the fp64 pipe fed. The projection kernel is launched as this
+// kernel's programmatic dependent: it may start at once, and only its
+// epilogue waits for the table.
+constexpr int kQkvTabPer = 4;
+
 __global__ void qkv_table_kernel(const int32_t* __restrict__ start_pos, int M, int T, int Tmax,
                                  float* __restrict__ cos_tab, float* __restrict__ sin_tab, int32_t* status) {
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)M * 64) return;
-  const int row = int(idx >> 6), j = int(idx & 63);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float s_inv[64];  // the 64 inverse frequencies, once per block (each is an fp64 power)
+  if (threadIdx.x < 64) s_inv[threadIdx.x] = rope_inv_freq(threadIdx.x);
+  __syncthreads();
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one (row, group of frequencies)
+  if (idx >= (long long)M * (64 / kQkvTabPer)) return;
+  const int row = int(idx / (64 / kQkvTabPer)), j0 = int(idx % (64 / kQkvTabPer)) * kQkvTabPer;
   const int b = row / T, i = row % T;
   const int s = __ldg(start_pos + b);
   if (s < 0 || (long long)s + T > Tmax) {
-    if (i == 0 && j == 0) report(status, GROK_DEV_BAD_START);
+    if (i == 0 && j0 == 0) report(status, GROK_DEV_BAD_START);
     return;
   }
-  float c, sn;
-  rope_cos_sin(__fmul_rn(float(s + i), rope_inv_freq(j)), c, sn);
-  cos_tab[idx] = c;
-  sin_tab[idx] = sn;
+  float c[kQkvTabPer], sn[kQkvTabPer];
+#pragma unroll
+  for (int u = 0; u < kQkvTabPer; ++u) rope_cos_sin(__fmul_rn(float(s + i), s_inv[j0 + u]), c[u], sn[u]);
+  float4* cp = reinterpret_cast<float4*>(cos_tab + (size_t)row * 64 + j0);
+  float4* sp = reinterpret_cast<float4*>(sin_tab + (size_t)row * 64 + j0);
+  *cp = make_float4(c[0], c[1], c[2], c[3]);
+  *sp = make_float4(sn[0], sn[1], sn[2], sn[3]);
 }
 
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
@@ -233,6 +248,9 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t tlane = uint32_t(quad * 32) << 16;
+    // The fused epilogue reads the cos / sin table of the kernel launched just
+    // before this one: wait for that grid (a no-op without a prerequisite).
+    if (kFused) asm volatile("griddepcontrol.wait;" ::: "memory");
     int tc = 0;
     for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tc) {
       int m, n;
@@ -347,7 +365,18 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[fused] = true;
   }
-  kernel<<<grid, kQkvThreads, kQkvSmem, static_cast<cudaStream_t>(stream)>>>(tx, tw, prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kQkvThreads);
+  cfg.dynamicSmemBytes = kQkvSmem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the table kernel before it
+  attr[0].val.programmaticStreamSerializationAllowed = fused ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, prm);
+  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "qkv launch: %s", cudaGetErrorString(e));
   return check_launch("qkv");
 }
 
@@ -403,7 +432,7 @@ extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16*
   prm.cache_k = reinterpret_cast<uint4*>(cache_k);
   prm.cache_v = reinterpret_cast<uint4*>(cache_v);
   prm.status = dev_status;
-  const long long total = M * 64;
+  const long long total = M * (64 / kQkvTabPer);
   qkv_table_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       start_pos, int(M), T, Tmax, const_cast<float*>(prm.cos_tab), const_cast<float*>(prm.sin_tab), dev_status);
   grok_status st = check_launch("qkv table");
