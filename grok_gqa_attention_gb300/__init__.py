@@ -45,6 +45,7 @@ EXPORTS = (
     "grok_qkv_project",
     "grok_qkv_workspace",
     "grok_qkv_rope_append",
+    "grok_linear",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -99,6 +100,8 @@ def load() -> ctypes.CDLL:
     lib.grok_qkv_workspace.argtypes = [I, I, ctypes.POINTER(S)]
     lib.grok_qkv_rope_append.restype = I
     lib.grok_qkv_rope_append.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P, P]
+    lib.grok_linear.restype = I
+    lib.grok_linear.argtypes = [P, P, I, I, I, P, P, P]
     _lib = lib
     return lib
 
@@ -334,3 +337,13 @@ def qkv_rope_append(x, w, start_pos, q_rot, cache_k, cache_v, workspace, dev_sta
     _check(load().grok_qkv_rope_append(_ptr(x), _ptr(w), _ptr(start_pos), B, T, Tmax, _ptr(q_rot), _ptr(cache_k),
                                        _ptr(cache_v), _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                        _stream(stream)))
+
+
+def linear(x, w, y, dev_status=None, stream=None) -> None:
+    """y [M, N] = x [M, K] . w [K, N] (bf16 Linear without bias; K % 64 == 0, N % 256 == 0)."""
+    M, K = x.shape
+    N = w.shape[1]
+    _want(x, "x", torch.bfloat16, (M, K))
+    _want(w, "w", torch.bfloat16, (K, N))
+    _want(y, "y", torch.bfloat16, (M, N))
+    _check(load().grok_linear(_ptr(x), _ptr(w), M, K, N, _ptr(y), _ptr(dev_status), _stream(stream)))

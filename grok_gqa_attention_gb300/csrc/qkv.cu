@@ -11,6 +11,10 @@
 // side by side, M = B * T rows (b * T + i). bf16 operands, fp32 accumulation
 // in TMEM, one rounding to bf16 per output. Output column h*128 + d is query
 // head h, 6144 + g*128 + d key head g, 7168 + g*128 + d value head g.
+// The same kernel with the plain epilogue is the general bias-free Linear
+// (grok_linear: any K that is a multiple of 64 and N of 256), which also
+// serves the output projection [M, 6144] . W_o [6144, 6144] and each
+// tensor-parallel rank's head slice of it.
 //
 // Persistent kernel, one CTA per SM, 6 warps:
 //   warp 0      TMA producer: per 64-wide K block one X box [128 rows x 64] and
@@ -43,8 +47,6 @@ constexpr int kQkvBM = 128, kQkvBN = 256, kQkvBK = 64;
 constexpr int kQkvStages = 4;
 constexpr int kQkvThreads = 192;
 constexpr int kQkvGroupM = 8;
-constexpr int kQkvKBlocks = kQkvK / kQkvBK;                 // 96
-constexpr int kQkvNTiles = kQkvN / kQkvBN;                  // 32
 constexpr int kQkvABytes = kQkvBM * kQkvBK * 2;             // 16 KB
 constexpr int kQkvBBox = kQkvBK * 64 * 2;                   // 8 KB: 64 K rows x 64 columns
 constexpr int kQkvBBytes = 4 * kQkvBBox;                    // 32 KB
@@ -60,11 +62,11 @@ struct QkvBars {
 constexpr int kQkvSmem = kQkvStages * kQkvStageBytes + int(sizeof(QkvBars)) + 1024;
 
 struct QkvParams {
-  int M, T, Tmax, n_mtiles, n_tiles;
+  int M, K, N, T, Tmax, n_mtiles, n_ntiles, k_blocks, n_tiles;
   const int32_t* start_pos;     // fused epilogue only
   const float* cos_tab;         // [M][64]
   const float* sin_tab;
-  uint4* y;                     // plain: [M][8192]
+  uint4* y;                     // plain: [M][N]
   uint4* q_rot;                 // fused: [B][T][48][128]
   uint4* cache_k;               // fused: [B][Tmax][8][128]
   uint4* cache_v;
@@ -72,7 +74,7 @@ struct QkvParams {
 };
 
 __device__ __forceinline__ void qkv_tile(const QkvParams& p, int t, int& m, int& n) {
-  const int per_group = kQkvGroupM * kQkvNTiles;
+  const int per_group = kQkvGroupM * p.n_ntiles;
   const int g = t / per_group, r = t % per_group;
   const int gm = min(kQkvGroupM, p.n_mtiles - g * kQkvGroupM);
   m = g * kQkvGroupM + r % gm;
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
         int m, n;
         qkv_tile(p, t, m, n);
-        for (int kb = 0; kb < kQkvKBlocks; ++kb, ++it) {
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int st = it % kQkvStages;
           if (!mbar_wait(&bars->empty[st], ((it / kQkvStages) & 1) ^ 1, abort, p.status)) {
             ok = false;
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[ab], ((tc >> 1) & 1) ^ 1, abort, p.status))) break;
       tc_fence_after();
       const uint32_t d = tmem + ab * kQkvBN;
-      for (int kb = 0; kb < kQkvKBlocks; ++kb, ++it) {
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
         const int st = it % kQkvStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[st], (it / kQkvStages) & 1, abort, p.status))) {
           ok = false;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       const int row = m * kQkvBM + r;
       const bool live = row < p.M;
       if (!kFused) {
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * kQkvN + n * kQkvBN) * 2;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * p.N + n * kQkvBN) * 2;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t a[32], o[16];
@@ -337,26 +339,31 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   }
 }
 
-grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, QkvParams& prm, void* stream) {
+grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, int K, int N, QkvParams& prm,
+                       void* stream) {
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
   CUtensorMap tx, tw;
   {
-    const uint64_t dims[4] = {uint64_t(kQkvK), uint64_t(M), 1, 1};
-    const uint64_t strides[3] = {uint64_t(kQkvK) * 2, uint64_t(kQkvK) * 2 * M, uint64_t(kQkvK) * 2 * M};
+    const uint64_t dims[4] = {uint64_t(K), uint64_t(M), 1, 1};
+    const uint64_t strides[3] = {uint64_t(K) * 2, uint64_t(K) * 2 * M, uint64_t(K) * 2 * M};
     const uint32_t box[4] = {uint32_t(kQkvBK), uint32_t(kQkvBM), 1, 1};
     if ((st = encode_tmap_bf16_4d(&tx, x, dims, strides, box)) != GROK_OK) return st;
   }
   {
-    const uint64_t dims[4] = {uint64_t(kQkvN), uint64_t(kQkvK), 1, 1};
-    const uint64_t strides[3] = {uint64_t(kQkvN) * 2, uint64_t(kQkvN) * 2 * kQkvK, uint64_t(kQkvN) * 2 * kQkvK};
+    const uint64_t dims[4] = {uint64_t(N), uint64_t(K), 1, 1};
+    const uint64_t strides[3] = {uint64_t(N) * 2, uint64_t(N) * 2 * K, uint64_t(N) * 2 * K};
     const uint32_t box[4] = {64, uint32_t(kQkvBK), 1, 1};
     if ((st = encode_tmap_bf16_4d(&tw, w, dims, strides, box)) != GROK_OK) return st;
   }
   prm.M = M;
+  prm.K = K;
+  prm.N = N;
+  prm.k_blocks = K / kQkvBK;
+  prm.n_ntiles = N / kQkvBN;
   prm.n_mtiles = (M + kQkvBM - 1) / kQkvBM;
-  prm.n_tiles = prm.n_mtiles * kQkvNTiles;
+  prm.n_tiles = prm.n_mtiles * prm.n_ntiles;
   const int grid = prm.n_tiles < sms ? prm.n_tiles : sms;
   auto kernel = fused ? qkv_kernel<true> : qkv_kernel<false>;
   static bool attr_set[2] = {false, false};  // idempotent: every thread would set the same value
@@ -384,18 +391,26 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
 
 using namespace grok;
 
-extern "C" grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y,
-                                        int32_t* dev_status, void* stream) {
-  if (!x || !w || !y) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: null pointer");
+extern "C" grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, int N, grok_bf16* y,
+                                   int32_t* dev_status, void* stream) {
+  if (!x || !w || !y) return fail(GROK_ERR_INVALID_ARG, "grok_linear: null pointer");
   if (!aligned16(x) || !aligned16(w) || !aligned16(y))
-    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: tensors must be 16-byte aligned");
-  if (M < 1) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_project: need M >= 1 (M=%d)", M);
+    return fail(GROK_ERR_INVALID_ARG, "grok_linear: tensors must be 16-byte aligned");
+  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || N < kQkvBN || N % kQkvBN != 0)
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_linear: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)", kQkvBK,
+                kQkvBN, M, K, N);
   QkvParams prm = {};
   prm.T = 1;
   prm.Tmax = 1;
   prm.y = reinterpret_cast<uint4*>(y);
   prm.status = dev_status;
-  return qkv_launch(false, x, w, M, prm, stream);
+  return qkv_launch(false, x, w, M, K, N, prm, stream);
+}
+
+extern "C" grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y,
+                                        int32_t* dev_status, void* stream) {
+  return grok_linear(x, w, M, kQkvK, kQkvN, y, dev_status, stream);
 }
 
 extern "C" grok_status grok_qkv_workspace(int B, int T, size_t* bytes) {
@@ -437,5 +452,5 @@ extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16*
       start_pos, int(M), T, Tmax, const_cast<float*>(prm.cos_tab), const_cast<float*>(prm.sin_tab), dev_status);
   grok_status st = check_launch("qkv table");
   if (st != GROK_OK) return st;
-  return qkv_launch(true, x, w, int(M), prm, stream);
+  return qkv_launch(true, x, w, int(M), kQkvK, kQkvN, prm, stream);
 }

@@ -216,6 +216,19 @@ grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16
  */
 grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y, int32_t* dev_status,
                              void* stream);
+
+/*
+ * A bias-free Linear (ch. 4 §4.1) on the same tensor-core kernel:
+ * y [M, N] = x [M, K] . w [K, N], bf16, fp32 accumulation, one rounding.
+ * K must be a positive multiple of 64 and N of 256; 1 <= M <= 2^30. Row-major,
+ * 16-byte aligned device tensors. Serves the output projection (ch. 4 §4.5.4:
+ * attention output [B*T, 48*128] head-major . W_o [6144, 6144]) and each
+ * tensor-parallel rank's share of it (the rows of W_o for the rank's heads,
+ * K = 6144 / ranks; the ranks' partial outputs are summed by the caller).
+ * grok_qkv_project is grok_linear with K = 6144, N = 8192.
+ */
+grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, int N, grok_bf16* y, int32_t* dev_status,
+                        void* stream);
 grok_status grok_qkv_workspace(int B, int T, size_t* bytes);
 grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B, int T,
                                  int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v, void* workspace,

@@ -13,6 +13,12 @@ reading I: RMSNorm, RoPE, GQA Attention" (yingwang.github.io/grok-1/04-model-1/)
 * §4.4 (RoPE placement): the projected query and key are then rotated with
   offset = the cache step and the rotated key and raw value written into the
   cache (``rope.rope_kv_append``).
+* §4.5.4 final projection: the attention output [B, T, 48, 128] is reshaped
+  to [B, T, 48 * 128] (heads in order h = 6g + r, features within a head
+  contiguous) and multiplied by a bias-free Linear to model_size 6144. The
+  Linear's weights are sharded along their input dimension (each model shard
+  holds the rows of its heads), so under tensor parallelism every shard
+  computes a partial product and the partials are summed.
 
 Readings where the pages leave details open:
 
@@ -69,3 +75,17 @@ def qkv_rope_append(x_bits, w_bits, start, cache_k_bits, cache_v_bits):
     """Projection, then §4.4's RoPE and cache append: returns (q_rot, new_cache_k, new_cache_v) bits."""
     q, k, v = qkv_projection(x_bits, w_bits)
     return rope.rope_kv_append(q, k, v, start, cache_k_bits, cache_v_bits)
+
+
+def output_projection(attn_bits: np.ndarray, w_o_bits: np.ndarray) -> np.ndarray:
+    """§4.5.4: attention output [B, T, 48, 128] flattened head-major, times W_o [6144, 6144] -> [B, T, 6144]."""
+    B, T = attn_bits.shape[0], attn_bits.shape[1]
+    return linear(attn_bits.reshape(B, T, N_Q_HEADS * HEAD_DIM), w_o_bits)
+
+
+def output_projection_partial(attn_bits: np.ndarray, w_o_bits: np.ndarray, rank: int, ranks: int) -> np.ndarray:
+    """One model shard's exact (fp64, unrounded) share: its heads' features times its rows of W_o."""
+    B, T = attn_bits.shape[0], attn_bits.shape[1]
+    width = N_Q_HEADS * HEAD_DIM // ranks
+    x = attn_bits.reshape(B, T, N_Q_HEADS * HEAD_DIM)[..., rank * width:(rank + 1) * width]
+    return linear_exact(x, w_o_bits[rank * width:(rank + 1) * width])

@@ -12,22 +12,29 @@ from oracle import bf16, projection as P, rope
 pytestmark = pytest.mark.gpu
 
 
-# The tensor cores accumulate the 6144-term dot in fp32: 384 additions of a
-# 16-term chunk into the accumulator, each rounding to half an fp32 ulp of a
-# partial sum. With |x| and |w| as generated, partial sums stay below 16, so
-# the accumulated error is at most 384 * 2^-20 = 3.7e-4 (typically ~1e-5).
-ACC_BOUND = 384 * 2.0 ** -20
+def acc_bound(K: int) -> float:
+    """The tensor cores accumulate a K-term dot in fp32: K/16 additions of a
+    16-term chunk into the accumulator, each rounding to half an fp32 ulp of a
+    partial sum. With the generated magnitudes partial sums stay below 16, so
+    the accumulated error is at most (K/16) * 2^-20 (K = 6144: 3.7e-4)."""
+    return (K // 16) * 2.0 ** -20
 
 
-def _projection_check(got_bits, exact, what, max_mismatch_frac=0.01):
+ACC_BOUND = acc_bound(6144)
+
+
+def _half_ulp(v):
+    return np.spacing(np.abs(v).astype(np.float32)).astype(np.float64) * 2 ** 15
+
+
+def _projection_check(got_bits, exact, what, max_mismatch_frac=0.01, K=6144):
     """Within half a bf16 ulp of the exact sum plus the fp32 accumulation bound;
     equal to the oracle's rounded bits for all but a small fraction."""
     g = bf16.to_f64(got_bits)
     assert np.all(np.isfinite(g))
-    mag = np.maximum(np.abs(exact), np.abs(g)).astype(np.float32)
-    half_ulp = np.spacing(mag).astype(np.float64) * 2 ** 15
+    half_ulp = np.maximum(_half_ulp(exact), _half_ulp(g))
     err = np.abs(g - exact)
-    assert np.all(err <= half_ulp + ACC_BOUND), f"{what}: worst excess {float((err - half_ulp).max())}"
+    assert np.all(err <= half_ulp + acc_bound(K)), f"{what}: worst excess {float((err - half_ulp).max())}"
     frac = float(np.mean(got_bits != bf16.from_f64(exact)))
     assert frac <= max_mismatch_frac, f"{what}: {frac:.4%} of outputs differ from the rounded exact sum"
     return frac
@@ -128,3 +135,58 @@ def test_argument_checks():
         G.qkv_rope_append(x, w, start, q_rot, ck, cv, small_ws)
     assert G.load().grok_qkv_project(None, None, 4, None, None, None) == 1
     assert G.qkv_workspace(B, T) == B * T * 64 * 2 * 4
+
+
+def _rand(gen, shape, scale):
+    return (torch.randn(*shape, generator=gen) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 64, 256), (130, 128, 512), (257, 6144, 256), (64, 768, 6144)])
+def test_linear_shapes_match_oracle(M, K, N):
+    gen = torch.Generator().manual_seed(M * 7 + K + N)
+    x = _rand(gen, (M, K), 1.0)
+    w = _rand(gen, (K, N), 3.0 / np.sqrt(K))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    G.linear(x.cuda(), w.cuda(), y)
+    torch.cuda.synchronize()
+    _projection_check(W.bits(y.cpu()), P.linear_exact(W.bits(x), W.bits(w)), f"linear {M}x{K}x{N}", K=K)
+
+
+@pytest.fixture(scope="module")
+def attn_out():
+    gen = torch.Generator().manual_seed(60)
+    attn = _rand(gen, (2, 200, 48, 128), 3.0)                 # an attention output [B, T, 48, 128]
+    w_o = _rand(gen, (6144, 6144), 1.0 / np.sqrt(6144))
+    return attn, w_o
+
+
+def test_output_projection_matches_oracle(attn_out):
+    attn, w_o = attn_out
+    y = torch.empty((400, 6144), dtype=torch.bfloat16, device="cuda")
+    G.linear(attn.reshape(400, 6144).cuda(), w_o.cuda(), y)
+    torch.cuda.synchronize()
+    exact = P.linear_exact(W.bits(attn).reshape(400, 6144), W.bits(w_o))
+    _projection_check(W.bits(y.cpu()), exact, "output projection M=400")
+
+
+def test_head_sharded_output_projection_partials_sum_to_the_whole(attn_out):
+    """Eight ranks, each holding 6 heads (768 features) and their 768 rows of W_o."""
+    attn, w_o = attn_out
+    ranks, width = 8, 768
+    a = attn.reshape(400, 6144)
+    total = np.zeros((400, 6144))
+    bound = np.zeros((400, 6144))
+    for r in range(ranks):
+        xr = a[:, r * width:(r + 1) * width].contiguous().cuda()
+        wr = w_o[r * width:(r + 1) * width].contiguous().cuda()
+        yr = torch.empty((400, 6144), dtype=torch.bfloat16, device="cuda")
+        G.linear(xr, wr, yr)
+        torch.cuda.synchronize()
+        got = W.bits(yr.cpu())
+        exact_r = P.output_projection_partial(W.bits(attn), W.bits(w_o), r, ranks).reshape(400, 6144)
+        _projection_check(got, exact_r, f"rank {r} partial", K=width)
+        g = bf16.to_f64(got)
+        total += g
+        bound += _half_ulp(g) + acc_bound(width)
+    whole = P.linear_exact(W.bits(a), W.bits(w_o))
+    assert np.all(np.abs(total - whole) <= bound + 1e-12)

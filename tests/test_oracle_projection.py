@@ -100,3 +100,25 @@ def test_fused_step_at_position_zero_keeps_the_projection():
     # at another position the rotation is the RoPE oracle's
     q_rot3, nk3, _ = P.qkv_rope_append(x, w, np.array([3]), ck, cv)
     assert np.array_equal(q_rot3, rope.rotary_embedding(q, np.array([3])))
+
+
+def test_output_projection_reads_heads_in_order():
+    """Input column h*128 + d of W_o multiplies head h, feature d of the attention output."""
+    rng = np.random.default_rng(26)
+    attn = _rand_bf16(rng, (1, 2, P.N_Q_HEADS, P.HEAD_DIM))
+    for h, d in [(0, 0), (5, 77), (47, 127)]:
+        w = np.zeros((P.N_Q_HEADS * P.HEAD_DIM, 256), dtype=np.uint16)
+        w[h * 128 + d, 3] = ONE
+        y = P.output_projection(attn, w)
+        assert np.array_equal(y[:, :, 3], attn[:, :, h, d])
+        assert not np.delete(y, 3, axis=-1).any()
+
+
+def test_output_projection_shards_sum_to_the_whole():
+    rng = np.random.default_rng(27)
+    attn = _rand_bf16(rng, (1, 3, P.N_Q_HEADS, P.HEAD_DIM))
+    w = _rand_bf16(rng, (P.N_Q_HEADS * P.HEAD_DIM, 256), 3.0 / np.sqrt(6144))
+    whole = P.linear_exact(attn.reshape(1, 3, -1), w)
+    for ranks in (2, 8):
+        parts = sum(P.output_projection_partial(attn, w, r, ranks) for r in range(ranks))
+        assert np.abs(parts - whole).max() < 1e-12
