@@ -472,6 +472,13 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
     ms_plain, t_plain = timed(lambda: G.qkv_project(x2d, w, y))
     ms_fused, t_fused = timed(lambda: G.qkv_rope_append(x, w, start, q_rot, ck, cv, ws, status))
     ms_cublas, _ = timed(lambda: torch.matmul(x2d, w))
+    # output projection (the step after the attention call): [M, 6144] . W_o [6144, 6144]
+    gen = torch.Generator().manual_seed(100 + rank)
+    w_o = (torch.randn(G.MODEL_SIZE, G.MODEL_SIZE, generator=gen) / np.sqrt(G.MODEL_SIZE)).to(torch.bfloat16).to(dev)
+    attn2d = q_rot.view(M, G.MODEL_SIZE)   # any [M, 6144] bf16 activation of the right scale
+    y_o = torch.empty((M, G.MODEL_SIZE), dtype=torch.bfloat16, device=dev)
+    ms_out, t_out = timed(lambda: G.linear(attn2d, w_o, y_o))
+    flops_out = 2.0 * M * G.MODEL_SIZE * G.MODEL_SIZE
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the projection")
@@ -488,13 +495,16 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_plain / peak_tf,
                      "peak_source": f"bf16_tflops ({peak_kind})", "traffic": measured_traffic("qkv_kernel"),
                      "traffic_unit": "bytes per launch (ncu)"},
+        "output_projection": {"shape": {"M": M, "K": G.MODEL_SIZE, "N": G.MODEL_SIZE}, "call": "grok_linear",
+                              "ms": ms_out, "TFLOP/s": flops_out / (ms_out * 1e-3) / 1e12,
+                              "frac": flops_out / (ms_out * 1e-3) / 1e12 / peak_tf, "stats": time_stats(t_out)},
         "cublas_context": {"op": "torch.matmul on the same bf16 product", "ms": ms_cublas,
                            "TFLOP/s": flops / (ms_cublas * 1e-3) / 1e12},
         "data": "synthetic (seeded randn -> bf16; weights randn*3/sqrt(6144))",
         "l2": "inputs larger than L2 (x 100 MB, W 100 MB, y 134 MB)",
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
     }
-    del x, w, ck, cv, y, q_rot
+    del x, w, ck, cv, y, q_rot, w_o, y_o
     torch.cuda.empty_cache()
     return out
 
