@@ -13,6 +13,12 @@ reading I: RMSNorm, RoPE, GQA Attention" (yingwang.github.io/grok-1/04-model-1/)
 * §4.4 (RoPE placement): the projected query and key are then rotated with
   offset = the cache step and the rotated key and raw value written into the
   cache (``rope.rope_kv_append``).
+* §4.1 Linear with ``QuantizedWeight8bit`` and §4.1.1: when the weight carries
+  ``scales``, the weight is dequantized as ``weight.astype(scales.dtype) *
+  scales`` (int8 weight [input, output], one fp32 scale per output channel,
+  broadcast along the input axis) and then cast to the input dtype before the
+  dot. Reading: the product is an fp32 multiply rounded to fp32, then rounded
+  to bf16 (two roundings, in the pages' order).
 * §4.5.4 final projection: the attention output [B, T, 48, 128] is reshaped
   to [B, T, 48 * 128] (heads in order h = 6g + r, features within a head
   contiguous) and multiplied by a bias-free Linear to model_size 6144. The
@@ -89,3 +95,14 @@ def output_projection_partial(attn_bits: np.ndarray, w_o_bits: np.ndarray, rank:
     width = N_Q_HEADS * HEAD_DIM // ranks
     x = attn_bits.reshape(B, T, N_Q_HEADS * HEAD_DIM)[..., rank * width:(rank + 1) * width]
     return linear_exact(x, w_o_bits[rank * width:(rank + 1) * width])
+
+
+def dequant_int8(w8: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """§4.1: int8 weight [K, N] times fp32 per-output-channel scales [N], rounded to fp32, then to bf16."""
+    prod = (w8.astype(np.float32) * scales.astype(np.float32)[None, :]).astype(np.float32)
+    return bf16.from_f32(prod)
+
+
+def linear_int8(x_bits: np.ndarray, w8: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """§4.1 Linear with a QuantizedWeight8bit weight: dequantize, then the bf16 dot."""
+    return linear(x_bits, dequant_int8(w8, scales))

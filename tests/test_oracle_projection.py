@@ -122,3 +122,38 @@ def test_output_projection_shards_sum_to_the_whole():
     for ranks in (2, 8):
         parts = sum(P.output_projection_partial(attn, w, r, ranks) for r in range(ranks))
         assert np.abs(parts - whole).max() < 1e-12
+
+
+def test_dequant_int8_matches_exact_products_rounded_twice():
+    """int8 (8 bits) x fp32 (24 bits) fits fp64 exactly, so float(w) * float(s) is the exact
+    product; np.float32 of it is the fp32 rounding and the brute-force search the bf16 one."""
+    rng = np.random.default_rng(28)
+    w8 = rng.integers(-128, 128, size=(6, 5)).astype(np.int8)
+    scales = (rng.random(5) * 1e-3 + 1e-4).astype(np.float32)
+    got = bf16.to_f64(P.dequant_int8(w8, scales))
+    for i in range(6):
+        for n in range(5):
+            exact = float(w8[i, n]) * float(scales[n])          # exact in fp64
+            r32 = float(np.float32(exact))
+            assert got[i, n] == _nearest_bf16_of_fraction(Fraction(r32))
+
+
+def test_dequant_int8_unit_and_power_of_two_scales_are_exact():
+    w8 = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(16, 16)
+    for s in (1.0, 0.25, 2.0 ** -10):
+        got = bf16.to_f64(P.dequant_int8(w8, np.full(16, s, dtype=np.float32)))
+        assert np.array_equal(got, w8.astype(np.float64) * s)
+
+
+def test_linear_int8_is_linear_on_the_dequantized_weight():
+    rng = np.random.default_rng(29)
+    x = _rand_bf16(rng, (1, 3, 64))
+    w8 = rng.integers(-127, 128, size=(64, 256)).astype(np.int8)
+    scales = (rng.random(256) * 0.01).astype(np.float32)
+    assert np.array_equal(P.linear_int8(x, w8, scales), P.linear(x, P.dequant_int8(w8, scales)))
+    # a per-channel scale only scales its own output column (power-of-two ratio: exact)
+    s2 = scales.copy()
+    s2[7] *= 4.0
+    a, b = bf16.to_f64(P.linear_int8(x, w8, scales)), bf16.to_f64(P.linear_int8(x, w8, s2))
+    assert np.array_equal(b[..., 7], 4.0 * a[..., 7])
+    assert np.array_equal(np.delete(a, 7, axis=-1), np.delete(b, 7, axis=-1))
