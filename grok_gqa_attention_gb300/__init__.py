@@ -46,6 +46,9 @@ EXPORTS = (
     "grok_qkv_workspace",
     "grok_qkv_rope_append",
     "grok_linear",
+    "grok_dequant_int8",
+    "grok_linear_int8_workspace",
+    "grok_linear_int8",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -102,6 +105,12 @@ def load() -> ctypes.CDLL:
     lib.grok_qkv_rope_append.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P, P]
     lib.grok_linear.restype = I
     lib.grok_linear.argtypes = [P, P, I, I, I, P, P, P]
+    lib.grok_dequant_int8.restype = I
+    lib.grok_dequant_int8.argtypes = [P, P, I, I, P, P]
+    lib.grok_linear_int8_workspace.restype = I
+    lib.grok_linear_int8_workspace.argtypes = [I, I, ctypes.POINTER(S)]
+    lib.grok_linear_int8.restype = I
+    lib.grok_linear_int8.argtypes = [P, P, P, I, I, I, P, P, S, P, P]
     _lib = lib
     return lib
 
@@ -347,3 +356,30 @@ def linear(x, w, y, dev_status=None, stream=None) -> None:
     _want(w, "w", torch.bfloat16, (K, N))
     _want(y, "y", torch.bfloat16, (M, N))
     _check(load().grok_linear(_ptr(x), _ptr(w), M, K, N, _ptr(y), _ptr(dev_status), _stream(stream)))
+
+
+def dequant_int8(w8, scales, w16, stream=None) -> None:
+    """w16 [K, N] bf16 = bf16(fp32(w8 [K, N] int8 * scales [N] fp32))."""
+    K, N = w8.shape
+    _want(w8, "w8", torch.int8, (K, N))
+    _want(scales, "scales", torch.float32, (N,))
+    _want(w16, "w16", torch.bfloat16, (K, N))
+    _check(load().grok_dequant_int8(_ptr(w8), _ptr(scales), K, N, _ptr(w16), _stream(stream)))
+
+
+def linear_int8_workspace(K: int, N: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().grok_linear_int8_workspace(int(K), int(N), ctypes.byref(n)))
+    return int(n.value)
+
+
+def linear_int8(x, w8, scales, y, workspace, dev_status=None, stream=None) -> None:
+    """y [M, N] = x [M, K] . dequant_int8(w8, scales) (see grok_linear_int8)."""
+    M, K = x.shape
+    N = w8.shape[1]
+    _want(x, "x", torch.bfloat16, (M, K))
+    _want(w8, "w8", torch.int8, (K, N))
+    _want(scales, "scales", torch.float32, (N,))
+    _want(y, "y", torch.bfloat16, (M, N))
+    _check(load().grok_linear_int8(_ptr(x), _ptr(w8), _ptr(scales), M, K, N, _ptr(y), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))

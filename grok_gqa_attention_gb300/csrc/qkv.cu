@@ -339,6 +339,38 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   }
 }
 
+// Int8 weight-only quantisation (ch. 4 §4.1, §4.1.1 QuantizedWeight8bit): the
+// weight is int8 [K, N] with one fp32 scale per output column, dequantized as
+// an fp32 product rounded to fp32, then rounded to bf16 (the pages' order:
+// astype(scales.dtype) * scales, then astype(bf16)). Each thread converts 16
+// consecutive weights of one row: one 16-byte load, two 16-byte stores.
+__global__ void dequant_int8_kernel(const uint4* __restrict__ w8, const float4* __restrict__ scales, long long chunks,
+                                    int N, uint4* __restrict__ w16) {
+  const int per_row = N / 16;
+  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
+       c += (long long)gridDim.x * blockDim.x) {
+    const int n0 = int(c % per_row) * 16;
+    const uint4 raw = __ldg(w8 + c);
+    const uint32_t word[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 sc = __ldg(scales + (n0 >> 2) + q);
+      const float sv[4] = {sc.x, sc.y, sc.z, sc.w};
+      float f[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int v = int(word[q] << (24 - 8 * b)) >> 24;  // sign-extended byte b
+        f[b] = __fmul_rn(float(v), sv[b]);
+      }
+      out[2 * q] = pack_bf16x2(f[0], f[1]);
+      out[2 * q + 1] = pack_bf16x2(f[2], f[3]);
+    }
+    w16[2 * c] = make_uint4(out[0], out[1], out[2], out[3]);
+    w16[2 * c + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
 grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, int K, int N, QkvParams& prm,
                        void* stream) {
   int sms = 0;
@@ -453,4 +485,49 @@ extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16*
   grok_status st = check_launch("qkv table");
   if (st != GROK_OK) return st;
   return qkv_launch(true, x, w, int(M), kQkvK, kQkvN, prm, stream);
+}
+
+extern "C" grok_status grok_dequant_int8(const int8_t* w8, const float* scales, int K, int N, grok_bf16* w16,
+                                         void* stream) {
+  if (!w8 || !scales || !w16) return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: null pointer");
+  if (!aligned16(w8) || !aligned16(scales) || !aligned16(w16))
+    return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: tensors must be 16-byte aligned");
+  if (K < 1 || N < 16 || N % 16 != 0)
+    return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: need K >= 1 and N a positive multiple of 16 (K=%d N=%d)", K,
+                N);
+  int sms = 0;
+  grok_status st = device_sm_count(&sms);
+  if (st != GROK_OK) return st;
+  const long long chunks = (long long)K * N / 16;
+  long long blocks = (chunks + 255) / 256;
+  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+  dequant_int8_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(w8), reinterpret_cast<const float4*>(scales), chunks, N,
+      reinterpret_cast<uint4*>(w16));
+  return check_launch("dequant_int8");
+}
+
+extern "C" grok_status grok_linear_int8_workspace(int K, int N, size_t* bytes) {
+  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8_workspace: null pointer");
+  if (K < 1 || N < 1) return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8_workspace: need K, N >= 1");
+  *bytes = size_t(K) * N * sizeof(grok_bf16);
+  return GROK_OK;
+}
+
+extern "C" grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, const float* scales, int M, int K,
+                                        int N, grok_bf16* y, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                        void* stream) {
+  if (!workspace) return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: null workspace");
+  if (ws_bytes < size_t(K) * N * sizeof(grok_bf16))
+    return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: workspace of %zu bytes, need %zu", ws_bytes,
+                size_t(K) * N * sizeof(grok_bf16));
+  // grok_linear's shape rules first, so that nothing is queued for a call it would reject
+  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || N < kQkvBN || N % kQkvBN != 0)
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_linear_int8: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)",
+                kQkvBK, kQkvBN, M, K, N);
+  grok_bf16* w16 = static_cast<grok_bf16*>(workspace);
+  grok_status st = grok_dequant_int8(w8, scales, K, N, w16, stream);
+  if (st != GROK_OK) return st;
+  return grok_linear(x, w16, M, K, N, y, dev_status, stream);
 }

@@ -229,6 +229,26 @@ grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok
  */
 grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, int N, grok_bf16* y, int32_t* dev_status,
                         void* stream);
+
+/*
+ * Int8 weight-only Linear (ch. 4 §4.1 Linear with QuantizedWeight8bit, §4.1.1):
+ * weight int8 [K, N] (row-major, the pages' [input, output] layout) with one
+ * fp32 scale per output column, scales [N].
+ * grok_dequant_int8: w16 [K, N] bf16 = bf16(fp32(w8 * scales[n])): an fp32
+ *   multiply rounded to fp32, then rounded to nearest even bf16 (the pages'
+ *   astype(scales.dtype) * scales, then astype(bf16)). N a multiple of 16.
+ * grok_linear_int8: y [M, N] = x [M, K] . dequant(w8, scales): the weight is
+ *   dequantized into the caller's workspace (at least
+ *   grok_linear_int8_workspace(K, N) bytes, K*N bf16) and then multiplied by
+ *   grok_linear (so K % 64 == 0, N % 256 == 0). For prefill-sized M the
+ *   product is tensor-bound and the one pass over the weight costs a few
+ *   percent; the workspace may be reused across calls with the same weight.
+ * All pointers device-resident and 16-byte aligned; asynchronous on stream.
+ */
+grok_status grok_dequant_int8(const int8_t* w8, const float* scales, int K, int N, grok_bf16* w16, void* stream);
+grok_status grok_linear_int8_workspace(int K, int N, size_t* bytes);
+grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, const float* scales, int M, int K, int N,
+                             grok_bf16* y, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 grok_status grok_qkv_workspace(int B, int T, size_t* bytes);
 grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B, int T,
                                  int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v, void* workspace,

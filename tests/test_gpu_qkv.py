@@ -190,3 +190,34 @@ def test_head_sharded_output_projection_partials_sum_to_the_whole(attn_out):
         bound += _half_ulp(g) + acc_bound(width)
     whole = P.linear_exact(W.bits(a), W.bits(w_o))
     assert np.all(np.abs(total - whole) <= bound + 1e-12)
+
+
+def _int8_weight(gen, K, N):
+    w8 = torch.randint(-127, 128, (K, N), generator=gen, dtype=torch.int32).to(torch.int8)
+    scales = (torch.rand(N, generator=gen) + 0.5) * (3.0 / np.sqrt(K) / 73.0)   # |w8| has std ~73
+    return w8, scales.to(torch.float32)
+
+
+@pytest.mark.parametrize("K,N", [(96, 48), (6144, 8192)])
+def test_dequant_int8_bit_exact(K, N):
+    gen = torch.Generator().manual_seed(K + N)
+    w8, scales = _int8_weight(gen, K, N)
+    w16 = torch.empty((K, N), dtype=torch.bfloat16, device="cuda")
+    G.dequant_int8(w8.cuda(), scales.cuda(), w16)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(w16.cpu()), P.dequant_int8(w8.numpy(), scales.numpy()))
+
+
+def test_linear_int8_matches_oracle():
+    gen = torch.Generator().manual_seed(70)
+    M, K, N = 130, 768, 512
+    x = _rand(gen, (M, K), 1.0)
+    w8, scales = _int8_weight(gen, K, N)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(G.linear_int8_workspace(K, N), dtype=torch.uint8, device="cuda")
+    G.linear_int8(x.cuda(), w8.cuda(), scales.cuda(), y, ws)
+    torch.cuda.synchronize()
+    w16 = P.dequant_int8(w8.numpy(), scales.numpy())
+    _projection_check(W.bits(y.cpu()), P.linear_exact(W.bits(x), w16), "int8 linear", K=K)
+    with pytest.raises(G.GrokError):   # workspace too small
+        G.linear_int8(x.cuda(), w8.cuda(), scales.cuda(), y, ws[:16])
