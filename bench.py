@@ -479,6 +479,13 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
     y_o = torch.empty((M, G.MODEL_SIZE), dtype=torch.bfloat16, device=dev)
     ms_out, t_out = timed(lambda: G.linear(attn2d, w_o, y_o))
     flops_out = 2.0 * M * G.MODEL_SIZE * G.MODEL_SIZE
+    # int8 weight-only Linear on the Q/K/V shape: dequantize (HBM-bound), then the bf16 product
+    w8 = torch.randint(-127, 128, (G.MODEL_SIZE, G.QKV_COLUMNS), generator=gen, dtype=torch.int32).to(torch.int8).to(dev)
+    scales = ((torch.rand(G.QKV_COLUMNS, generator=gen) + 0.5) * (3.0 / np.sqrt(G.MODEL_SIZE) / 73.0)).to(dev)
+    w16 = torch.empty((G.MODEL_SIZE, G.QKV_COLUMNS), dtype=torch.bfloat16, device=dev)
+    ms_deq, _ = timed(lambda: G.dequant_int8(w8, scales, w16))
+    ms_i8, _ = timed(lambda: G.linear_int8(x2d, w8, scales, y, w16))
+    deq_bytes = G.MODEL_SIZE * G.QKV_COLUMNS * 3 + G.QKV_COLUMNS * 4
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the projection")
@@ -498,13 +505,17 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
         "output_projection": {"shape": {"M": M, "K": G.MODEL_SIZE, "N": G.MODEL_SIZE}, "call": "grok_linear",
                               "ms": ms_out, "TFLOP/s": flops_out / (ms_out * 1e-3) / 1e12,
                               "frac": flops_out / (ms_out * 1e-3) / 1e12 / peak_tf, "stats": time_stats(t_out)},
+        "int8_linear": {"call": "grok_linear_int8 (grok_dequant_int8 into a workspace, then grok_linear)",
+                        "ms": ms_i8, "TFLOP/s": flops / (ms_i8 * 1e-3) / 1e12,
+                        "dequant_ms": ms_deq, "dequant_GB/s": deq_bytes / (ms_deq * 1e-3) / 1e9,
+                        "dequant_frac_of_hbm": deq_bytes / (ms_deq * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))},
         "cublas_context": {"op": "torch.matmul on the same bf16 product", "ms": ms_cublas,
                            "TFLOP/s": flops / (ms_cublas * 1e-3) / 1e12},
         "data": "synthetic (seeded randn -> bf16; weights randn*3/sqrt(6144))",
         "l2": "inputs larger than L2 (x 100 MB, W 100 MB, y 134 MB)",
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 7 * args.steps,
     }
-    del x, w, ck, cv, y, q_rot, w_o, y_o
+    del x, w, ck, cv, y, q_rot, w_o, y_o, w8, w16
     torch.cuda.empty_cache()
     return out
 

@@ -344,30 +344,37 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
 // an fp32 product rounded to fp32, then rounded to bf16 (the pages' order:
 // astype(scales.dtype) * scales, then astype(bf16)). Each thread converts 16
 // consecutive weights of one row: one 16-byte load, two 16-byte stores.
+__device__ __forceinline__ void dequant16(uint4 raw, const float4* __restrict__ scales, int n0, uint4* dst) {
+  const uint32_t word[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 sc = __ldg(scales + (n0 >> 2) + q);
+    const float sv[4] = {sc.x, sc.y, sc.z, sc.w};
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int v = int(word[q] << (24 - 8 * b)) >> 24;  // sign-extended byte b
+      f[b] = __fmul_rn(float(v), sv[b]);
+    }
+    out[2 * q] = pack_bf16x2(f[0], f[1]);
+    out[2 * q + 1] = pack_bf16x2(f[2], f[3]);
+  }
+  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// Two chunks per thread per pass, both loads issued before either converts.
 __global__ void dequant_int8_kernel(const uint4* __restrict__ w8, const float4* __restrict__ scales, long long chunks,
                                     int N, uint4* __restrict__ w16) {
   const int per_row = N / 16;
-  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks;
-       c += (long long)gridDim.x * blockDim.x) {
-    const int n0 = int(c % per_row) * 16;
-    const uint4 raw = __ldg(w8 + c);
-    const uint32_t word[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t out[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 sc = __ldg(scales + (n0 >> 2) + q);
-      const float sv[4] = {sc.x, sc.y, sc.z, sc.w};
-      float f[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int v = int(word[q] << (24 - 8 * b)) >> 24;  // sign-extended byte b
-        f[b] = __fmul_rn(float(v), sv[b]);
-      }
-      out[2 * q] = pack_bf16x2(f[0], f[1]);
-      out[2 * q + 1] = pack_bf16x2(f[2], f[3]);
-    }
-    w16[2 * c] = make_uint4(out[0], out[1], out[2], out[3]);
-    w16[2 * c + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += 2 * stride) {
+    const long long c2 = c + stride;
+    const uint4 r1 = __ldg(w8 + c);
+    const uint4 r2 = c2 < chunks ? __ldg(w8 + c2) : make_uint4(0, 0, 0, 0);
+    dequant16(r1, scales, int(c % per_row) * 16, w16 + 2 * c);
+    if (c2 < chunks) dequant16(r2, scales, int(c2 % per_row) * 16, w16 + 2 * c2);
   }
 }
 
