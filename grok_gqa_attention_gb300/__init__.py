@@ -24,6 +24,9 @@ DEV_BAD_START = 0x1
 DEV_BAD_VALID = 0x2
 DEV_BAD_KV_LEN = 0x4
 DEV_TIMEOUT = 0x8
+DEV_BAD_PAGE = 0x10
+
+PAGE_TOKENS = 128
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgrok_attn.so")
 
@@ -49,6 +52,9 @@ EXPORTS = (
     "grok_dequant_int8",
     "grok_linear_int8_workspace",
     "grok_linear_int8",
+    "grok_rope_kv_append_paged",
+    "grok_attn_prefill_paged",
+    "grok_attn_decode_paged",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -111,6 +117,12 @@ def load() -> ctypes.CDLL:
     lib.grok_linear_int8_workspace.argtypes = [I, I, ctypes.POINTER(S)]
     lib.grok_linear_int8.restype = I
     lib.grok_linear_int8.argtypes = [P, P, P, I, I, I, P, P, S, P, P]
+    lib.grok_rope_kv_append_paged.restype = I
+    lib.grok_rope_kv_append_paged.argtypes = [P, P, P, P, I, I, P, P, P, I, P, I, P, P]
+    lib.grok_attn_prefill_paged.restype = I
+    lib.grok_attn_prefill_paged.argtypes = [P, P, P, I, P, I, P, P, I, I, P, P, P]
+    lib.grok_attn_decode_paged.restype = I
+    lib.grok_attn_decode_paged.argtypes = [P, P, P, I, P, I, P, I, P, S, P, P]
     _lib = lib
     return lib
 
@@ -383,3 +395,65 @@ def linear_int8(x, w8, scales, y, workspace, dev_status=None, stream=None) -> No
     _want(y, "y", torch.bfloat16, (M, N))
     _check(load().grok_linear_int8(_ptr(x), _ptr(w8), _ptr(scales), M, K, N, _ptr(y), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def _want_pages(k_pool, v_pool, block_table, B: int) -> tuple[int, int]:
+    """Checks a paged cache (pools [n_pages, 128, 8, 128], table [B, max_pages]); returns (n_pages, max_pages)."""
+    n_pages = k_pool.shape[0]
+    _want(k_pool, "k_pool", torch.bfloat16, (n_pages, PAGE_TOKENS, N_KV_HEADS, HEAD_DIM))
+    _want(v_pool, "v_pool", torch.bfloat16, (n_pages, PAGE_TOKENS, N_KV_HEADS, HEAD_DIM))
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B, max_pages]")
+    max_pages = block_table.shape[1]
+    _want(block_table, "block_table", torch.int32, (B, max_pages))
+    return n_pages, max_pages
+
+
+def rope_kv_append_paged(q, k, v, start_pos, q_rot, k_pool, v_pool, block_table, dev_status=None,
+                         stream=None) -> None:
+    """rope_kv_append into a paged cache: position p of sequence b goes to row p % 128 of page block_table[b, p // 128]."""
+    B, T = q.shape[0], q.shape[1]
+    _want(q, "q", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(k, "k", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(v, "v", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    n_pages, max_pages = _want_pages(k_pool, v_pool, block_table, B)
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_rope_kv_append_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), B, T, _ptr(q_rot),
+                                            _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table), max_pages,
+                                            _ptr(dev_status), _stream(stream)))
+
+
+def prefill_paged(q_rot, k_pool, v_pool, block_table, start_pos, valid_len, out, dev_status=None,
+                  stream=None) -> None:
+    """prefill() over a paged cache (valid_len may be None)."""
+    B, T = q_rot.shape[0], q_rot.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    n_pages, max_pages = _want_pages(k_pool, v_pool, block_table, B)
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    if valid_len is not None:
+        _want(valid_len, "valid_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_attn_prefill_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table),
+                                          max_pages, _ptr(start_pos), _ptr(valid_len), B, T, _ptr(out),
+                                          _ptr(dev_status), _stream(stream)))
+
+
+def decode_paged(q_rot, k_pool, v_pool, block_table, kv_len, workspace, dev_status=None, stream=None) -> None:
+    """decode() over a paged cache; combine() it with Tmax = block_table.shape[1] * PAGE_TOKENS."""
+    B = q_rot.shape[0]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    n_pages, max_pages = _want_pages(k_pool, v_pool, block_table, B)
+    _want(kv_len, "kv_len", torch.int32, (B,))
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().grok_attn_decode_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table),
+                                         max_pages, _ptr(kv_len), B, _ptr(workspace), nbytes, _ptr(dev_status),
+                                         _stream(stream)))

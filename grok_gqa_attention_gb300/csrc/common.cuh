@@ -45,6 +45,41 @@ __device__ __forceinline__ void report(int32_t* status, int32_t code) {
 }
 
 // ----------------------------------------------------------------------------
+// KV-cache addressing. Contiguous: cache [B][Tmax][8][128], row (b, key).
+// Paged: a pool [n_pages][GROK_PAGE_TOKENS][8][128] and a block table
+// [B][max_pages] of page ids; key `key` of sequence b is row key % 128 of page
+// table[b][key / 128]. As TMA coordinates: (row, b) contiguous, (page * 128 +
+// key % 128, 0) paged. A page id outside [0, n_pages) reports
+// GROK_DEV_BAD_PAGE and resolves to page 0 (a load stays in bounds; callers
+// that store check kv_page_ok first).
+struct PageMap {
+  const int32_t* table;  // nullptr: contiguous cache
+  int max_pages;
+  int n_pages;
+};
+
+__device__ __forceinline__ bool kv_page_ok(const PageMap& pm, int b, int key) {
+  if (!pm.table) return true;
+  const int pg = __ldg(pm.table + (size_t)b * pm.max_pages + (key / GROK_PAGE_TOKENS));
+  return pg >= 0 && pg < pm.n_pages;
+}
+
+__device__ __forceinline__ void kv_coord(const PageMap& pm, int b, int key, int& row, int& bc, int32_t* status) {
+  if (!pm.table) {
+    row = key;
+    bc = b;
+    return;
+  }
+  int pg = __ldg(pm.table + (size_t)b * pm.max_pages + (key / GROK_PAGE_TOKENS));
+  if (pg < 0 || pg >= pm.n_pages) {
+    report(status, GROK_DEV_BAD_PAGE);
+    pg = 0;
+  }
+  row = pg * GROK_PAGE_TOKENS + key % GROK_PAGE_TOKENS;
+  bc = 0;
+}
+
+// ----------------------------------------------------------------------------
 // shared-memory addresses, mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

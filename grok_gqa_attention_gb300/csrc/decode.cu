@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap tm_v,
                                                              const uint32_t* __restrict__ q_rot,
                                                              const int32_t* __restrict__ kv_len, int Tmax,
-                                                             int n_split, DecWs ws, int32_t* status) {
+                                                             int n_split, DecWs ws, PageMap pm, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes);
@@ -86,11 +86,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     for (int s = 0; s < kDecStages && s < n_st; ++s) {
       uint8_t* base = smem + s * kDecStageBytes;
       const int key0 = k0 + s * kDecKeysPerStage;
+      int row, bc;
+      kv_coord(pm, b, key0, row, bc, status);  // a 64-key tile never straddles a page
       mbar_arrive_expect_tx(&full[s], kDecStageBytes);
-      tma_load_4d(base, &tm_k, &full[s], 0, g, key0, b);
-      tma_load_4d(base + kDecBox, &tm_k, &full[s], 64, g, key0, b);
-      tma_load_4d(base + 2 * kDecBox, &tm_v, &full[s], 0, g, key0, b);
-      tma_load_4d(base + 3 * kDecBox, &tm_v, &full[s], 64, g, key0, b);
+      tma_load_4d(base, &tm_k, &full[s], 0, g, row, bc);
+      tma_load_4d(base + kDecBox, &tm_k, &full[s], 64, g, row, bc);
+      tma_load_4d(base + 2 * kDecBox, &tm_v, &full[s], 0, g, row, bc);
+      tma_load_4d(base + 3 * kDecBox, &tm_v, &full[s], 64, g, row, bc);
     }
   }
 
@@ -186,11 +188,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       if (mbar_wait(&empty[st], (it / kDecStages) & 1, abort, status)) {
         uint8_t* base = smem + st * kDecStageBytes;
         const int key0 = k0 + (it + kDecStages) * kDecKeysPerStage;
+        int row, bc;
+        kv_coord(pm, b, key0, row, bc, status);
         mbar_arrive_expect_tx(&full[st], kDecStageBytes);
-        tma_load_4d(base, &tm_k, &full[st], 0, g, key0, b);
-        tma_load_4d(base + kDecBox, &tm_k, &full[st], 64, g, key0, b);
-        tma_load_4d(base + 2 * kDecBox, &tm_v, &full[st], 0, g, key0, b);
-        tma_load_4d(base + 3 * kDecBox, &tm_v, &full[st], 64, g, key0, b);
+        tma_load_4d(base, &tm_k, &full[st], 0, g, row, bc);
+        tma_load_4d(base + kDecBox, &tm_k, &full[st], 64, g, row, bc);
+        tma_load_4d(base + 2 * kDecBox, &tm_v, &full[st], 0, g, row, bc);
+        tma_load_4d(base + 3 * kDecBox, &tm_v, &full[st], 64, g, row, bc);
       }
     }
   }
@@ -285,6 +289,31 @@ static grok_status decode_args(const void* ws, size_t ws_bytes, const int32_t* k
   return GROK_OK;
 }
 
+static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
+                                 uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* kv_len, int B,
+                                 int Tmax, void* workspace, int32_t* dev_status, void* stream) {
+  grok_status st;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != GROK_OK) return st;
+  const int ns = (Tmax + kDecSplit - 1) / kDecSplit;
+  CUtensorMap tk, tv;
+  const uint64_t dims[4] = {kD, kKVHeads, kv_rows, kv_seqs};
+  const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, kv_rows * kKVHeads * kD * 2};
+  const uint32_t box[4] = {64, 1, kDecKeysPerStage, 1};
+  if ((st = encode_tmap_bf16_4d(&tk, k_src, dims, strides, box)) != GROK_OK) return st;
+  if ((st = encode_tmap_bf16_4d(&tv, v_src, dims, strides, box)) != GROK_OK) return st;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    attr_set = true;
+  }
+  const dim3 grid(ns, kKVHeads, B);
+  decode_kernel<<<grid, kDecThreads, kDecSmem, static_cast<cudaStream_t>(stream)>>>(
+      tk, tv, reinterpret_cast<const uint32_t*>(q_rot), kv_len, Tmax, ns, dec_ws(workspace, B, ns), pm, dev_status);
+  return check_launch("decode");
+}
+
 extern "C" grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k,
                                         const grok_bf16* cache_v, const int32_t* kv_len, int B, int Tmax,
                                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
@@ -294,25 +323,29 @@ extern "C" grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16*
     return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode: bf16 tensors must be 16-byte aligned");
   grok_status st = decode_args(workspace, workspace_bytes, kv_len, B, Tmax, "grok_attn_decode");
   if (st != GROK_OK) return st;
-  int sms = 0;
-  if ((st = device_sm_count(&sms)) != GROK_OK) return st;
-  const int ns = (Tmax + kDecSplit - 1) / kDecSplit;
-  CUtensorMap tk, tv;
-  const uint64_t dims[4] = {kD, kKVHeads, uint64_t(Tmax), uint64_t(B)};
-  const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, uint64_t(Tmax) * kKVHeads * kD * 2};
-  const uint32_t box[4] = {64, 1, kDecKeysPerStage, 1};
-  if ((st = encode_tmap_bf16_4d(&tk, cache_k, dims, strides, box)) != GROK_OK) return st;
-  if ((st = encode_tmap_bf16_4d(&tv, cache_v, dims, strides, box)) != GROK_OK) return st;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set = true;
-  }
-  const dim3 grid(ns, kKVHeads, B);
-  decode_kernel<<<grid, kDecThreads, kDecSmem, static_cast<cudaStream_t>(stream)>>>(
-      tk, tv, reinterpret_cast<const uint32_t*>(q_rot), kv_len, Tmax, ns, dec_ws(workspace, B, ns), dev_status);
-  return check_launch("decode");
+  return decode_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, kv_len, B, Tmax,
+                       workspace, dev_status, stream);
+}
+
+extern "C" grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok_bf16* k_pool,
+                                              const grok_bf16* v_pool, int n_pages, const int32_t* block_table,
+                                              int max_pages, const int32_t* kv_len, int B, void* workspace,
+                                              size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!q_rot || !k_pool || !v_pool || !block_table)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_paged: null pointer");
+  if (!aligned16(q_rot) || !aligned16(k_pool) || !aligned16(v_pool))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_paged: bf16 tensors must be 16-byte aligned");
+  if (n_pages < 1 || max_pages < 1 || (long long)n_pages * GROK_PAGE_TOKENS > (1LL << 31))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_paged: need n_pages, max_pages >= 1 (n_pages=%d, max_pages=%d)",
+                n_pages, max_pages);
+  const long long Tmax = (long long)max_pages * GROK_PAGE_TOKENS;
+  if (Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_paged: max_pages * %d must be <= %d", GROK_PAGE_TOKENS,
+                GROK_MAX_POSITION);
+  grok_status st = decode_args(workspace, workspace_bytes, kv_len, B, int(Tmax), "grok_attn_decode_paged");
+  if (st != GROK_OK) return st;
+  return decode_launch(q_rot, k_pool, v_pool, uint64_t(n_pages) * GROK_PAGE_TOKENS, 1,
+                       PageMap{block_table, max_pages, n_pages}, kv_len, B, int(Tmax), workspace, dev_status, stream);
 }
 
 extern "C" grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len,

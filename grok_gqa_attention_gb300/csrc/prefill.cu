@@ -82,6 +82,7 @@ constexpr int kPfSmem = kPfData + int(sizeof(PfBars)) + 1024;
 
 struct PfParams {
   int B, T, Tmax, n_qt, n_items;
+  PageMap pm;  // K/V addressing (contiguous cache or paged pool)
   const int32_t* start_pos;
   const int32_t* valid_len;
   int32_t* status;
@@ -314,16 +315,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ok = false;
             break;
           }
+          int krow, kb;
+          kv_coord(p.pm, it.b, j * kPfKeys, krow, kb, p.status);  // a tile is one page when paged
           mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
-          tma_load_4d(sK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, it.g, j * kPfKeys, it.b);
-          tma_load_4d(sK + st * kTileBytes + kBox, &tm_k, &bars->k_full[st], 64, it.g, j * kPfKeys, it.b);
+          tma_load_4d(sK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, it.g, krow, kb);
+          tma_load_4d(sK + st * kTileBytes + kBox, &tm_k, &bars->k_full[st], 64, it.g, krow, kb);
           if (!mbar_wait(&bars->v_empty[st], par, abort, p.status)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-          tma_load_4d(sV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, it.g, j * kPfKeys, it.b);
-          tma_load_4d(sV + st * kTileBytes + kBox, &tm_v, &bars->v_full[st], 64, it.g, j * kPfKeys, it.b);
+          tma_load_4d(sV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, it.g, krow, kb);
+          tma_load_4d(sV + st * kTileBytes + kBox, &tm_v, &bars->v_full[st], 64, it.g, krow, kb);
         }
         if (!ok) break;
       }
@@ -558,17 +561,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 using namespace grok;
 
-extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k,
-                                         const grok_bf16* cache_v, const int32_t* start_pos,
-                                         const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
-                                         int32_t* dev_status, void* stream) {
-  if (!q_rot || !cache_k || !cache_v || !start_pos || !out)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: null pointer");
-  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: bf16 tensors must be 16-byte aligned");
-  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
-                GROK_MAX_POSITION, B, T, Tmax);
+static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
+                                  uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* start_pos,
+                                  const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out, int32_t* dev_status,
+                                  void* stream) {
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
@@ -583,15 +579,16 @@ extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16
     if ((st = encode_tmap_bf16_4d(&to, out, dims, strides, obox)) != GROK_OK) return st;
   }
   {
-    const uint64_t dims[4] = {kD, kKVHeads, uint64_t(Tmax), uint64_t(B)};
-    const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, uint64_t(Tmax) * kKVHeads * kD * 2};
-    if ((st = encode_tmap_bf16_4d(&tk, cache_k, dims, strides, box)) != GROK_OK) return st;
-    if ((st = encode_tmap_bf16_4d(&tv, cache_v, dims, strides, box)) != GROK_OK) return st;
+    const uint64_t dims[4] = {kD, kKVHeads, kv_rows, kv_seqs};
+    const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, kv_rows * kKVHeads * kD * 2};
+    if ((st = encode_tmap_bf16_4d(&tk, k_src, dims, strides, box)) != GROK_OK) return st;
+    if ((st = encode_tmap_bf16_4d(&tv, v_src, dims, strides, box)) != GROK_OK) return st;
   }
   PfParams prm;
   prm.B = B;
   prm.T = T;
   prm.Tmax = Tmax;
+  prm.pm = pm;
   prm.n_qt = (T + kPfRows - 1) / kPfRows;
   prm.n_items = prm.n_qt * B * kKVHeads * 3;
   prm.start_pos = start_pos;
@@ -607,4 +604,39 @@ extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16
   const int grid = prm.n_items < sms ? prm.n_items : sms;
   prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
   return check_launch("prefill");
+}
+
+extern "C" grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k,
+                                         const grok_bf16* cache_v, const int32_t* start_pos,
+                                         const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
+                                         int32_t* dev_status, void* stream) {
+  if (!q_rot || !cache_k || !cache_v || !start_pos || !out)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: null pointer");
+  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: bf16 tensors must be 16-byte aligned");
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+                GROK_MAX_POSITION, B, T, Tmax);
+  return prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                        valid_len, B, T, Tmax, out, dev_status, stream);
+}
+
+extern "C" grok_status grok_attn_prefill_paged(const grok_bf16* q_rot, const grok_bf16* k_pool,
+                                               const grok_bf16* v_pool, int n_pages, const int32_t* block_table,
+                                               int max_pages, const int32_t* start_pos, const int32_t* valid_len,
+                                               int B, int T, grok_bf16* out, int32_t* dev_status, void* stream) {
+  if (!q_rot || !k_pool || !v_pool || !block_table || !start_pos || !out)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_paged: null pointer");
+  if (!aligned16(q_rot) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_paged: bf16 tensors must be 16-byte aligned");
+  const long long Tmax = (long long)max_pages * GROK_PAGE_TOKENS;
+  if (B < 1 || T < 1 || n_pages < 1 || max_pages < 1 || T > Tmax || Tmax > GROK_MAX_POSITION ||
+      (long long)n_pages * GROK_PAGE_TOKENS > (1LL << 31))
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_attn_prefill_paged: need B, T, n_pages, max_pages >= 1, T <= max_pages * %d <= %d "
+                "(B=%d T=%d max_pages=%d n_pages=%d)",
+                GROK_PAGE_TOKENS, GROK_MAX_POSITION, B, T, max_pages, n_pages);
+  return prefill_launch(q_rot, k_pool, v_pool, uint64_t(n_pages) * GROK_PAGE_TOKENS, 1,
+                        PageMap{block_table, max_pages, n_pages}, start_pos, valid_len, B, T, int(Tmax), out,
+                        dev_status, stream);
 }

@@ -57,7 +57,7 @@ template <int team>
 __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int32_t* __restrict__ start_pos, int B, int T, int Tmax, uint4* __restrict__ q_rot,
-    uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, int32_t* status) {
+    uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, PageMap pm, int32_t* status) {
   __shared__ float s_inv[64];
   __shared__ float s_cos[kRopeWarps][64];
   __shared__ float s_sin[kRopeWarps][64];
@@ -82,7 +82,16 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
     rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
     __syncwarp();
-    const size_t row = (size_t)b * Tmax + pos;
+    // cache row of (b, pos): contiguous b * Tmax + pos, paged page * 128 + pos % 128; a
+    // token whose page id is out of range still gets its q_rot but no cache write
+    size_t row = (size_t)b * Tmax + pos;
+    bool kv_ok = true;
+    if (pm.table) {
+      const int pg = __ldg(pm.table + (size_t)b * pm.max_pages + pos / GROK_PAGE_TOKENS);
+      kv_ok = pg >= 0 && pg < pm.n_pages;
+      if (!kv_ok && lane == 0 && member == 0) report(status, GROK_DEV_BAD_PAGE);
+      row = (size_t)(kv_ok ? pg : 0) * GROK_PAGE_TOKENS + pos % GROK_PAGE_TOKENS;
+    }
     const uint4* qsrc = q + (size_t)tok * kQHeads * 16;
     const uint4* ksrc = k + (size_t)tok * kKVHeads * 16;
     uint4* qdst = q_rot + (size_t)tok * kQHeads * 16;
@@ -105,6 +114,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     for (int m = 0; m < 14; ++m) {
       if (m % team != member) continue;
       const int u = lane + 32 * m, head = u >> 3, c = u & 7;
+      if (head >= kQHeads && !kv_ok) continue;
       uint4 y1, y2;
       rotate8(x1[m], x2[m], &s_cos[warp][8 * c], &s_sin[warp][8 * c], y1, y2);
       uint4* dst = head < kQHeads ? qdst + head * 16 : kdst + (head - kQHeads) * 16;
@@ -113,7 +123,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      if (m % team == member) cache_v[row * (kKVHeads * 16) + lane + 32 * m] = vv[m];
+      if (m % team == member && kv_ok) cache_v[row * (kKVHeads * 16) + lane + 32 * m] = vv[m];
   }
 }
 
@@ -134,19 +144,18 @@ __global__ void rope_table_kernel(int p0, int n, float* __restrict__ cos_out, fl
 
 using namespace grok;
 
-extern "C" grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
-                                           const int32_t* start_pos, int B, int T, int Tmax, grok_bf16* q_rot,
-                                           grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status,
-                                           void* stream) {
+static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                 const int32_t* start_pos, int B, int T, int Tmax, grok_bf16* q_rot,
+                                 grok_bf16* cache_k, grok_bf16* cache_v, PageMap pm, int32_t* dev_status,
+                                 void* stream, const char* name) {
   if (!q || !k || !v || !start_pos || !q_rot || !cache_k || !cache_v)
-    return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append: null pointer");
+    return fail(GROK_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(cache_k) ||
       !aligned16(cache_v))
-    return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append: bf16 tensors must be 16-byte aligned");
+    return fail(GROK_ERR_INVALID_ARG, "%s: bf16 tensors must be 16-byte aligned", name);
   if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || T > GROK_MAX_POSITION)
-    return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append: need B >= 1, 1 <= T <= Tmax (B=%d T=%d Tmax=%d)", B,
-                T, Tmax);
-  if (q == q_rot) return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append: q_rot may not alias q");
+    return fail(GROK_ERR_INVALID_ARG, "%s: need B >= 1, 1 <= T <= Tmax (B=%d T=%d Tmax=%d)", name, B, T, Tmax);
+  if (q == q_rot) return fail(GROK_ERR_INVALID_ARG, "%s: q_rot may not alias q", name);
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
@@ -163,8 +172,32 @@ extern "C" grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* 
   kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
       start_pos, B, T, Tmax, reinterpret_cast<uint4*>(q_rot), reinterpret_cast<uint4*>(cache_k),
-      reinterpret_cast<uint4*>(cache_v), dev_status);
+      reinterpret_cast<uint4*>(cache_v), pm, dev_status);
   return check_launch("rope_kv_append");
+}
+
+extern "C" grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                           const int32_t* start_pos, int B, int T, int Tmax, grok_bf16* q_rot,
+                                           grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status,
+                                           void* stream) {
+  return append_launch(q, k, v, start_pos, B, T, Tmax, q_rot, cache_k, cache_v, PageMap{nullptr, 0, 0}, dev_status,
+                       stream, "grok_rope_kv_append");
+}
+
+extern "C" grok_status grok_rope_kv_append_paged(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                                 const int32_t* start_pos, int B, int T, grok_bf16* q_rot,
+                                                 grok_bf16* k_pool, grok_bf16* v_pool, int n_pages,
+                                                 const int32_t* block_table, int max_pages, int32_t* dev_status,
+                                                 void* stream) {
+  if (!block_table) return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append_paged: null block table");
+  if (n_pages < 1 || max_pages < 1 || (long long)n_pages * GROK_PAGE_TOKENS > (1LL << 31) ||
+      (long long)max_pages * GROK_PAGE_TOKENS > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_rope_kv_append_paged: need n_pages, max_pages >= 1, max_pages * %d <= %d "
+                "(n_pages=%d max_pages=%d)",
+                GROK_PAGE_TOKENS, GROK_MAX_POSITION, n_pages, max_pages);
+  return append_launch(q, k, v, start_pos, B, T, max_pages * GROK_PAGE_TOKENS, q_rot, k_pool, v_pool,
+                       PageMap{block_table, max_pages, n_pages}, dev_status, stream, "grok_rope_kv_append_paged");
 }
 
 extern "C" grok_status grok_rope_cos_sin(int first_position, int n_positions, float* cos_out, float* sin_out,

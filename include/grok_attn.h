@@ -68,6 +68,10 @@ typedef enum {
 #define GROK_DEV_BAD_VALID 0x2   /* valid_len[b] outside [1, T] */
 #define GROK_DEV_BAD_KV_LEN 0x4  /* kv_len[b] outside [1, Tmax] */
 #define GROK_DEV_TIMEOUT 0x8     /* a bounded wait inside a kernel gave up */
+#define GROK_DEV_BAD_PAGE 0x10   /* a block-table entry the paged calls need lies outside [0, n_pages) */
+
+/* Tokens per page of the paged KV cache (one prefill key tile). */
+#define GROK_PAGE_TOKENS 128
 
 /* ABI version this library was built with (GROK_ATTN_ABI_VERSION). */
 int grok_abi_version(void);
@@ -292,6 +296,53 @@ grok_status grok_prefill_pipe_submit(grok_prefill_pipe* pipe, const grok_bf16* q
                                      grok_bf16* out);
 grok_status grok_prefill_pipe_wait(grok_prefill_pipe* pipe, int32_t* dev_status);
 grok_status grok_prefill_pipe_destroy(grok_prefill_pipe* pipe);
+
+/*
+ * Paged KV cache (code-reading guide ch. 6 "model.py close reading II": §6.6
+ * preallocates the cache at (B, 8192, 8, 128); §6.6.1 gives every sequence its
+ * own step counter so sequences can join and leave a batch independently;
+ * §6.6.2 notes that serving systems store the cache in token pages that are
+ * allocated only when used, which Grok-1's code does not do). These calls are
+ * the contiguous calls above with the cache rows looked up through a block
+ * table; the arithmetic, and so every result bit, is the same as for a
+ * contiguous cache holding the same keys and values.
+ *
+ * Layout: k_pool, v_pool [n_pages, GROK_PAGE_TOKENS, 8, 128] bf16, 16-byte
+ * aligned, owned by the caller. block_table [B, max_pages] int32 (device):
+ * position p of sequence b lives in row p % GROK_PAGE_TOKENS of page
+ * block_table[b * max_pages + p / GROK_PAGE_TOKENS]. A sequence's capacity is
+ * max_pages * GROK_PAGE_TOKENS (it plays the part of Tmax, at most
+ * GROK_MAX_POSITION). Pages may be shared between sequences and listed in any
+ * order; table entries past what a call touches are never read, so unused
+ * entries may hold anything. Every table entry a call reads must lie in
+ * [0, n_pages): otherwise the call sets GROK_DEV_BAD_PAGE, reads page 0 in
+ * its place (results for that sequence are then meaningless) and the append
+ * skips that token's cache write (its q_rot is still written).
+ *
+ * grok_rope_kv_append_paged: grok_rope_kv_append writing rows
+ *   [start_pos[b], start_pos[b] + T) of sequence b through the table.
+ * grok_attn_prefill_paged: grok_attn_prefill reading keys [0, start_pos[b] +
+ *   valid_len[b]) of sequence b through the table.
+ * grok_attn_decode_paged: grok_attn_decode reading keys [0, kv_len[b]) through
+ *   the table; workspace sized by grok_attn_decode_workspace(B, max_pages *
+ *   GROK_PAGE_TOKENS) and combined with grok_attn_combine(..., Tmax = max_pages
+ *   * GROK_PAGE_TOKENS, ...).
+ * Argument errors (null pointers, misaligned tensors, n_pages < 1,
+ * max_pages < 1, sizes past the limits above) return GROK_ERR_INVALID_ARG with
+ * nothing launched.
+ */
+grok_status grok_rope_kv_append_paged(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                      const int32_t* start_pos, int B, int T, grok_bf16* q_rot, grok_bf16* k_pool,
+                                      grok_bf16* v_pool, int n_pages, const int32_t* block_table, int max_pages,
+                                      int32_t* dev_status, void* stream);
+grok_status grok_attn_prefill_paged(const grok_bf16* q_rot, const grok_bf16* k_pool, const grok_bf16* v_pool,
+                                    int n_pages, const int32_t* block_table, int max_pages,
+                                    const int32_t* start_pos, const int32_t* valid_len, int B, int T,
+                                    grok_bf16* out, int32_t* dev_status, void* stream);
+grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok_bf16* k_pool, const grok_bf16* v_pool,
+                                   int n_pages, const int32_t* block_table, int max_pages, const int32_t* kv_len,
+                                   int B, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   void* stream);
 
 #ifdef __cplusplus
 }

@@ -209,3 +209,60 @@ def projection(B: int, T: int, Tmax: int, start_pos, seed: int = 0, junk: str = 
     junk_rows_(cache_k, start, junk)
     junk_rows_(cache_v, start, junk)
     return ProjectionInputs(x, w, cache_k, cache_v, start)
+
+
+PAGE_TOKENS = 128
+
+
+def page_table(B: int, max_pages: int, need, spare: int = 3, seed: int = 0, unused: int = -1):
+    """A block table [B, max_pages] int32 over a pool of n_pages, and n_pages.
+
+    Sequence b gets need[b] pages, drawn without replacement from the pool in a
+    seeded random order (so logical neighbours are scattered); the pool holds
+    `spare` pages that no sequence uses; table entries past need[b] hold `unused`.
+    """
+    need = np.asarray(need, dtype=np.int64)
+    if need.shape != (B,) or (need < 0).any() or (need > max_pages).any():
+        raise ValueError("need[b] must lie in [0, max_pages]")
+    n_pages = int(need.sum()) + spare
+    perm = np.random.default_rng(seed).permutation(n_pages)
+    table = np.full((B, max_pages), unused, dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[at:at + need[b]]
+        at += need[b]
+    return torch.from_numpy(table), n_pages
+
+
+def pages_needed(end_positions) -> np.ndarray:
+    """Pages that hold positions [0, end) for each end."""
+    end = np.asarray(end_positions, dtype=np.int64)
+    return (end + PAGE_TOKENS - 1) // PAGE_TOKENS
+
+
+def to_pages(cache: torch.Tensor, table: torch.Tensor, n_pages: int, seed: int = 0) -> torch.Tensor:
+    """Scatter a contiguous cache [B, Tmax, 8, 128] into a pool [n_pages, 128, 8, 128].
+
+    Page table[b, j] receives rows [128 j, 128 j + 128) of sequence b (rows past
+    Tmax stay as filler); pages no entry names are seeded random filler.
+    """
+    B, Tmax = cache.shape[0], cache.shape[1]
+    gen = torch.Generator().manual_seed(seed)
+    pool = _randn_bf16(gen, (n_pages, PAGE_TOKENS) + tuple(cache.shape[2:]), 3.0)
+    for b in range(B):
+        for j, pg in enumerate(table[b].tolist()):
+            if 0 <= pg < n_pages:
+                lo = j * PAGE_TOKENS
+                hi = min(lo + PAGE_TOKENS, Tmax)
+                if lo < hi:
+                    pool[pg, :hi - lo] = cache[b, lo:hi]
+    return pool
+
+
+def from_pages(pool: torch.Tensor, table: torch.Tensor, b: int, n_rows: int) -> torch.Tensor:
+    """Rows [0, n_rows) of sequence b gathered from a pool through the table."""
+    rows = []
+    for j in range((n_rows + PAGE_TOKENS - 1) // PAGE_TOKENS):
+        pg = int(table[b, j])
+        rows.append(pool[pg, :min(PAGE_TOKENS, n_rows - j * PAGE_TOKENS)])
+    return torch.cat(rows, 0)
