@@ -48,6 +48,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-qkv", action="store_true")
+    ap.add_argument("--no-paged", action="store_true", help="skip the paged-cache timings")
     ap.add_argument("--only", choices=["prefill", "decode", "qkv"], default=None,
                     help="run one workload only (profiling); implies --no-cpu-baseline --no-e2e")
     return ap.parse_args()
@@ -427,7 +428,105 @@ def run_ours(args, rank: int, world: int, dist):
     # ---------------- decode workload
     if not args.no_decode:
         result["decode"] = run_decode(args, rank, world, dist, dev, peaks, peak_kind)
+
+    # ---------------- paged KV cache: the same kernels through a shuffled block table
+    if not args.no_paged:
+        result["paged"] = run_paged(args, rank, dev)
     return result
+
+
+def _to_pool(cache, table, n_pages):
+    """Device-side scatter of a contiguous cache [B, Tmax, 8, 128] into pages (Tmax a multiple of 128)."""
+    import torch
+    B, Tmax = cache.shape[0], cache.shape[1]
+    pages = cache.reshape(B * (Tmax // 128), 128, cache.shape[2], cache.shape[3])
+    pool = torch.empty((n_pages, 128, cache.shape[2], cache.shape[3]), dtype=cache.dtype, device=cache.device)
+    pool[table.reshape(-1).long().to(cache.device)] = pages
+    return pool
+
+
+def run_paged(args, rank, dev):
+    """Kernel time of the paged calls against the contiguous calls on the same keys and values.
+
+    Every page of the caches is placed at a random slot of a pool (a full random
+    permutation), so consecutive key tiles of a sequence come from unrelated
+    addresses. Eager launches alternate between the two layouts; CUDA events
+    bracket each launch.
+    """
+    import torch
+
+    import grok_gqa_attention_gb300 as G
+    import workloads as W
+    res = {}
+    stream = torch.cuda.current_stream()
+    n = max(4, min(args.steps, 20))
+
+    def timed(fn):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b_.record(stream)
+        return a, b_
+
+    # prefill
+    inp = W.generate(PREFILL_WORKLOAD, seed=rank)
+    B, T, Tmax = inp.workload.B, inp.workload.T, inp.workload.Tmax
+    q_rot = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=dev)
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    valid = None if inp.valid_len is None else inp.valid_len.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    G.rope_kv_append(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), start, q_rot, ck, cv, status)
+    table, n_pages = W.page_table(B, Tmax // 128, [Tmax // 128] * B, spare=0, seed=100 + rank)
+    kp, vp, tab = _to_pool(ck, table, n_pages), _to_pool(cv, table, n_pages), table.to(dev)
+    out_c, out_p = torch.empty_like(q_rot), torch.empty_like(q_rot)
+    for _ in range(2):
+        G.prefill(q_rot, ck, cv, start, valid, out_c, status)
+        G.prefill_paged(q_rot, kp, vp, tab, start, valid, out_p, status)
+    ev_c, ev_p = [], []
+    for _ in range(n):
+        ev_c.append(timed(lambda: G.prefill(q_rot, ck, cv, start, valid, out_c, status)))
+        ev_p.append(timed(lambda: G.prefill_paged(q_rot, kp, vp, tab, start, valid, out_p, status)))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the paged prefill")
+    same = bool(torch.equal(out_c.view(torch.int16), out_p.view(torch.int16)))
+    mc = float(np.median([a.elapsed_time(b_) for a, b_ in ev_c]))
+    mp = float(np.median([a.elapsed_time(b_) for a, b_ in ev_p]))
+    res["prefill"] = {"workload": PREFILL_WORKLOAD, "pages": n_pages, "ms_contiguous": mc, "ms_paged": mp,
+                      "paged_over_contiguous": mp / mc, "bit_identical": same}
+    del q_rot, ck, cv, kp, vp, out_c, out_p
+    torch.cuda.empty_cache()
+
+    # decode
+    inp = W.generate(DECODE_WORKLOAD, seed=rank)
+    B, Tmax = inp.workload.B, inp.workload.Tmax
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    kv_len = (inp.start_pos + 1).to(torch.int32).to(dev)
+    q_rot = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=dev)
+    G.rope_kv_append(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), start, q_rot, ck, cv, status)
+    q1 = q_rot[:, 0].contiguous()
+    table, n_pages = W.page_table(B, Tmax // 128, [Tmax // 128] * B, spare=0, seed=200 + rank)
+    kp, vp, tab = _to_pool(ck, table, n_pages), _to_pool(cv, table, n_pages), table.to(dev)
+    ws = G.alloc_decode_workspace(B, Tmax, dev)
+    for _ in range(2):
+        G.decode(q1, ck, cv, kv_len, ws, status)
+        G.decode_paged(q1, kp, vp, tab, kv_len, ws, status)
+    ev_c, ev_p = [], []
+    for _ in range(n):
+        ev_c.append(timed(lambda: G.decode(q1, ck, cv, kv_len, ws, status)))
+        ev_p.append(timed(lambda: G.decode_paged(q1, kp, vp, tab, kv_len, ws, status)))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the paged decode")
+    mc = float(np.median([a.elapsed_time(b_) for a, b_ in ev_c]))
+    mp = float(np.median([a.elapsed_time(b_) for a, b_ in ev_p]))
+    nbytes = decode_bytes((inp.start_pos + 1).numpy())
+    res["decode"] = {"workload": DECODE_WORKLOAD, "pages": n_pages, "ms_contiguous": mc, "ms_paged": mp,
+                     "paged_over_contiguous": mp / mc, "GB/s_paged": nbytes / (mp * 1e-3) / 1e9}
+    res["gpu_launches"] = 4 * n + 8
+    return res
 
 
 QKV_WORKLOAD = (1, 8192)  # B, T of the projection line: the prefill workload's tokens
@@ -648,6 +747,7 @@ def main():
         args.no_e2e = True
         args.no_decode = args.only != "decode"
         args.no_qkv = args.only != "qkv"
+        args.no_paged = True
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
