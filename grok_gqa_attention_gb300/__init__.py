@@ -55,6 +55,7 @@ EXPORTS = (
     "grok_rope_kv_append_paged",
     "grok_attn_prefill_paged",
     "grok_attn_decode_paged",
+    "grok_qkv_rope_append_paged",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -123,6 +124,8 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_prefill_paged.argtypes = [P, P, P, I, P, I, P, P, I, I, P, P, P]
     lib.grok_attn_decode_paged.restype = I
     lib.grok_attn_decode_paged.argtypes = [P, P, P, I, P, I, P, I, P, S, P, P]
+    lib.grok_qkv_rope_append_paged.restype = I
+    lib.grok_qkv_rope_append_paged.argtypes = [P, P, P, I, I, P, P, P, I, P, I, P, S, P, P]
     _lib = lib
     return lib
 
@@ -457,3 +460,22 @@ def decode_paged(q_rot, k_pool, v_pool, block_table, kv_len, workspace, dev_stat
     _check(load().grok_attn_decode_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table),
                                          max_pages, _ptr(kv_len), B, _ptr(workspace), nbytes, _ptr(dev_status),
                                          _stream(stream)))
+
+
+def qkv_rope_append_paged(x, w, start_pos, q_rot, k_pool, v_pool, block_table, workspace, dev_status=None,
+                          stream=None) -> None:
+    """qkv_rope_append writing the k and v rows into a paged cache through the block table."""
+    B, T = x.shape[0], x.shape[1]
+    _want(x, "x", torch.bfloat16, (B, T, MODEL_SIZE))
+    _want(w, "w", torch.bfloat16, (MODEL_SIZE, QKV_COLUMNS))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    n_pages, max_pages = _want_pages(k_pool, v_pool, block_table, B)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().grok_qkv_rope_append_paged(_ptr(x), _ptr(w), _ptr(start_pos), B, T, _ptr(q_rot), _ptr(k_pool),
+                                             _ptr(v_pool), n_pages, _ptr(block_table), max_pages, _ptr(workspace),
+                                             nbytes, _ptr(dev_status), _stream(stream)))

@@ -29,7 +29,8 @@
 // blocks by all 32 column blocks, so the tiles in flight share X and W in L2.
 //
 // Epilogues: plain (write Y) or fused (q heads: RoPE -> q_rot; k heads: RoPE
-// -> cache_k at row start_pos[b] + i; v heads -> cache_v). The rotation is the
+// -> cache_k at row start_pos[b] + i, or at its page of a paged pool; v heads
+// -> cache_v). The rotation is the
 // one of rope_kv_append (separately rounded fp32 products and sum of the bf16
 // value and the fp32 cos / sin) with cos / sin taken from a per-step table
 // that qkv_table_kernel fills with the shared fp64 routine. The projection is
@@ -70,6 +71,7 @@ struct QkvParams {
   uint4* q_rot;                 // fused: [B][T][48][128]
   uint4* cache_k;               // fused: [B][Tmax][8][128]
   uint4* cache_v;
+  PageMap pm;                   // fused: cache rows through a block table (null: contiguous)
   int32_t* status;
 };
 
@@ -281,19 +283,30 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         const int b = row / p.T, i = row % p.T;
         const int s = live ? __ldg(p.start_pos + b) : 0;
         const bool write = live && s >= 0 && (long long)s + p.T <= p.Tmax;
+        // cache row of position s + i: contiguous b * Tmax + s + i; paged page * 128 + (s + i) % 128
+        size_t crow = (size_t)b * p.Tmax + s + i;
+        bool kv_write = write;
+        if (p.pm.table && write) {
+          const int pos = s + i;
+          const int pg = __ldg(p.pm.table + (size_t)b * p.pm.max_pages + pos / GROK_PAGE_TOKENS);
+          kv_write = pg >= 0 && pg < p.pm.n_pages;
+          if (!kv_write) report(p.status, GROK_DEV_BAD_PAGE);
+          crow = (size_t)(kv_write ? pg : 0) * GROK_PAGE_TOKENS + pos % GROK_PAGE_TOKENS;
+        }
         const bool rotate = n < (kQHeads + kKVHeads) * kD / kQkvBN;     // query and key columns
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {   // the tile's two heads
           const int col = n * kQkvBN + hh * kD;   // first output column of the head
           uint8_t* dst;
+          const bool store = col < kQHeads * kD ? write : kv_write;
           if (col < kQHeads * kD) {
             dst = reinterpret_cast<uint8_t*>(p.q_rot) + ((size_t)row * kQHeads * kD + col) * 2;
           } else if (col < (kQHeads + kKVHeads) * kD) {
             const int g = (col - kQHeads * kD) / kD;
-            dst = reinterpret_cast<uint8_t*>(p.cache_k) + ((((size_t)b * p.Tmax + s + i) * kKVHeads + g) * kD) * 2;
+            dst = reinterpret_cast<uint8_t*>(p.cache_k) + ((crow * kKVHeads + g) * kD) * 2;
           } else {
             const int g = (col - (kQHeads + kKVHeads) * kD) / kD;
-            dst = reinterpret_cast<uint8_t*>(p.cache_v) + ((((size_t)b * p.Tmax + s + i) * kKVHeads + g) * kD) * 2;
+            dst = reinterpret_cast<uint8_t*>(p.cache_v) + ((crow * kKVHeads + g) * kD) * 2;
           }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {   // features 32c .. 32c+31 paired with 64+32c ..
@@ -316,7 +329,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
               }
               qkv_rotate32(x1, x2, cs, sn);
             }
-            if (write) {
+            if (store) {
               st_global_v8(dst + c * 64, x1);
               st_global_v8(dst + c * 64 + 32, x1 + 8);
               st_global_v8(dst + 128 + c * 64, x2);
@@ -459,23 +472,23 @@ extern "C" grok_status grok_qkv_workspace(int B, int T, size_t* bytes) {
   return GROK_OK;
 }
 
-extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
-                                            int T, int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v,
-                                            void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
+                                          int T, int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v,
+                                          PageMap pm, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                          void* stream, const char* name) {
   if (!x || !w || !start_pos || !q_rot || !cache_k || !cache_v || !workspace)
-    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: null pointer");
+    return fail(GROK_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) ||
       !aligned16(workspace))
-    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: tensors must be 16-byte aligned");
+    return fail(GROK_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
   if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
-    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+    return fail(GROK_ERR_INVALID_ARG, "%s: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)", name,
                 GROK_MAX_POSITION, B, T, Tmax);
   size_t need = 0;
   grok_qkv_workspace(B, T, &need);
-  if (ws_bytes < need)
-    return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: workspace of %zu bytes, need %zu", ws_bytes, need);
+  if (ws_bytes < need) return fail(GROK_ERR_INVALID_ARG, "%s: workspace of %zu bytes, need %zu", name, ws_bytes, need);
   const long long M = (long long)B * T;
-  if (M > (1LL << 30)) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append: B * T too large");
+  if (M > (1LL << 30)) return fail(GROK_ERR_INVALID_ARG, "%s: B * T too large", name);
   QkvParams prm = {};
   prm.T = T;
   prm.Tmax = Tmax;
@@ -485,6 +498,7 @@ extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16*
   prm.q_rot = reinterpret_cast<uint4*>(q_rot);
   prm.cache_k = reinterpret_cast<uint4*>(cache_k);
   prm.cache_v = reinterpret_cast<uint4*>(cache_v);
+  prm.pm = pm;
   prm.status = dev_status;
   const long long total = M * (64 / kQkvTabPer);
   qkv_table_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
@@ -492,6 +506,30 @@ extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16*
   grok_status st = check_launch("qkv table");
   if (st != GROK_OK) return st;
   return qkv_launch(true, x, w, int(M), kQkvK, kQkvN, prm, stream);
+}
+
+extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
+                                            int T, int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v,
+                                            void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return qkv_rope_append_launch(x, w, start_pos, B, T, Tmax, q_rot, cache_k, cache_v, PageMap{nullptr, 0, 0},
+                                workspace, ws_bytes, dev_status, stream, "grok_qkv_rope_append");
+}
+
+extern "C" grok_status grok_qkv_rope_append_paged(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos,
+                                                  int B, int T, grok_bf16* q_rot, grok_bf16* k_pool,
+                                                  grok_bf16* v_pool, int n_pages, const int32_t* block_table,
+                                                  int max_pages, void* workspace, size_t ws_bytes,
+                                                  int32_t* dev_status, void* stream) {
+  if (!block_table) return fail(GROK_ERR_INVALID_ARG, "grok_qkv_rope_append_paged: null block table");
+  if (n_pages < 1 || max_pages < 1 || (long long)n_pages * GROK_PAGE_TOKENS > (1LL << 31) ||
+      (long long)max_pages * GROK_PAGE_TOKENS > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_qkv_rope_append_paged: need n_pages, max_pages >= 1, max_pages * %d <= %d "
+                "(n_pages=%d max_pages=%d)",
+                GROK_PAGE_TOKENS, GROK_MAX_POSITION, n_pages, max_pages);
+  return qkv_rope_append_launch(x, w, start_pos, B, T, max_pages * GROK_PAGE_TOKENS, q_rot, k_pool, v_pool,
+                                PageMap{block_table, max_pages, n_pages}, workspace, ws_bytes, dev_status, stream,
+                                "grok_qkv_rope_append_paged");
 }
 
 extern "C" grok_status grok_dequant_int8(const int8_t* w8, const float* scales, int K, int N, grok_bf16* w16,

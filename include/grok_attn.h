@@ -327,6 +327,9 @@ grok_status grok_prefill_pipe_destroy(grok_prefill_pipe* pipe);
  *   the table; workspace sized by grok_attn_decode_workspace(B, max_pages *
  *   GROK_PAGE_TOKENS) and combined with grok_attn_combine(..., Tmax = max_pages
  *   * GROK_PAGE_TOKENS, ...).
+ * grok_qkv_rope_append_paged: grok_qkv_rope_append (the projection fused with
+ *   RoPE and the append) writing the k and v rows through the table; the
+ *   workspace is sized by grok_qkv_workspace(B, T).
  * Argument errors (null pointers, misaligned tensors, n_pages < 1,
  * max_pages < 1, sizes past the limits above) return GROK_ERR_INVALID_ARG with
  * nothing launched.
@@ -343,6 +346,10 @@ grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok_bf16* k_po
                                    int n_pages, const int32_t* block_table, int max_pages, const int32_t* kv_len,
                                    int B, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                    void* stream);
+grok_status grok_qkv_rope_append_paged(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
+                                       int T, grok_bf16* q_rot, grok_bf16* k_pool, grok_bf16* v_pool, int n_pages,
+                                       const int32_t* block_table, int max_pages, void* workspace, size_t ws_bytes,
+                                       int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

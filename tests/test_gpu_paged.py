@@ -213,3 +213,41 @@ def test_paged_argument_errors():
                                          s) == 1
     with pytest.raises(ValueError):
         G.decode_paged(q_rot, kp, kp[:1], table, kv, ws)  # pools of different sizes
+
+
+def test_paged_fused_projection_matches_contiguous():
+    """The projection + RoPE + append epilogue writes the same rows through the table."""
+    B, T, Tmax = 2, 200, 512
+    pin = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[0, 130], seed=81)
+    x, w = pin.x.to(DEV), pin.w.to(DEV)
+    start = pin.start_pos.to(DEV)
+    ws = G.alloc_qkv_workspace(B, T, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ck, cv = pin.cache_k.to(DEV), pin.cache_v.to(DEV)
+    q_c = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device=DEV)
+    G.qkv_rope_append(x, w, start, q_c, ck, cv, ws, status)
+
+    end = pin.start_pos.numpy() + T
+    table, n_pages = W.page_table(B, Tmax // P, W.pages_needed(end), spare=2, seed=82)
+    kp0 = W.to_pages(pin.cache_k, table, n_pages, seed=83)
+    vp0 = W.to_pages(pin.cache_v, table, n_pages, seed=84)
+    kp, vp, tab = kp0.to(DEV), vp0.to(DEV), table.to(DEV)
+    q_p = torch.empty_like(q_c)
+    G.qkv_rope_append_paged(x, w, start, q_p, kp, vp, tab, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(W.bits(q_p.cpu()), W.bits(q_c.cpu()))
+    rk, rv = W.bits(ck.cpu()), W.bits(cv.cpu())
+    for b in range(B):
+        n = int(end[b])
+        assert np.array_equal(_gathered(kp, table, b, n), rk[b, :n]), f"k pages of sequence {b}"
+        assert np.array_equal(_gathered(vp, table, b, n), rv[b, :n]), f"v pages of sequence {b}"
+
+    bad = table.clone()
+    bad[1, 2] = -1  # positions 256..329 of sequence 1
+    kp, vp = kp0.to(DEV), vp0.to(DEV)
+    G.qkv_rope_append_paged(x, w, start, q_p, kp, vp, bad.to(DEV), ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & G.DEV_BAD_PAGE
+    assert np.array_equal(W.bits(q_p.cpu()), W.bits(q_c.cpu()))  # q_rot is still written
+    assert np.array_equal(W.bits(kp[table[1, 2]].cpu()), W.bits(kp0[table[1, 2]]))  # the page is untouched
