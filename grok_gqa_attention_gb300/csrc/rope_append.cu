@@ -7,11 +7,13 @@
 // update_into at step[b]).
 //
 // A team of 1, 2, 4 or 8 warps handles one token (b, i) (more warps per token
-// when there are few tokens): each warp evaluates the 64 (cos, sin) pairs of
-// the token's position in fp64 and rounds them to fp32, then streams its share
-// of the token's 48 query heads and 8 key heads (128-bit loads of 8 bf16 of the
-// first half and the matching 8 of the second half) and of its 8 value heads. The rotation uses separately rounded fp32 multiplies and adds
-// (no FMA contraction), so the result is bit-for-bit the fp32 chain.
+// when there are few tokens): each warp loads its share of the token's 48
+// query heads and 8 key heads (128-bit loads of 8 bf16 of the first half and
+// the matching 8 of the second half) and of its 8 value heads, evaluates the
+// 64 (cos, sin) pairs of the token's position in fp64 (rounded to fp32) while
+// those loads are in flight, then rotates and stores. The rotation uses
+// separately rounded fp32 multiplies and adds (no FMA contraction), so the
+// result is bit-for-bit the fp32 chain.
 //
 // Memory-bound: per token it reads 14 KB (q, k, v) and writes 14 KB.
 #include "common.cuh"
@@ -45,12 +47,14 @@ __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const 
 }
 
 // A team of `team` warps (1, 2, 4 or 8) per token, grid-stride over tokens
-// with no CTA-wide barrier: every warp of the team evaluates the token's 64
-// (cos, sin) pairs into its own shared-memory slice, then warp w of the team
-// takes the rotation units (8 pairs of one head) and value units whose index m
-// satisfies m % team == w, unrolled so that its loads are in flight together.
-// Large batches use one warp per token; a handful of tokens (a decode step)
-// spreads each token over eight warps.
+// with no CTA-wide barrier. Warp w of the team takes the rotation units (8
+// pairs of one head) and value units whose index m satisfies m % team == w: it
+// issues all their loads first, then evaluates the token's 64 (cos, sin) pairs
+// in fp64 into its own shared-memory slice while the loads are in flight (the
+// fp64 work, slow on this part, overlaps the memory latency instead of
+// preceding it), then rotates and stores. Large batches use one warp per
+// token; a handful of tokens (a decode step) spreads each token over eight
+// warps.
 constexpr int kRopeWarps = kRopeThreads / 32;
 
 template <int team>
@@ -78,10 +82,6 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
       continue;
     }
     const int pos = s0 + i;
-    __syncwarp();  // the previous token's table is no longer read
-    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
-    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
-    __syncwarp();
     // cache row of (b, pos): contiguous b * Tmax + pos, paged page * 128 + pos % 128; a
     // token whose page id is out of range still gets its q_rot but no cache write
     size_t row = (size_t)b * Tmax + pos;
@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (m % team == member) vv[m] = __ldg(v + (size_t)tok * (kKVHeads * 16) + lane + 32 * m);
+    __syncwarp();  // the previous token's table is no longer read
+    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
+    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
+    __syncwarp();
 #pragma unroll
     for (int m = 0; m < 14; ++m) {
       if (m % team != member) continue;
