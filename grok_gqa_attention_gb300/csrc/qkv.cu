@@ -85,34 +85,41 @@ __device__ __forceinline__ void qkv_tile(const QkvParams& p, int t, int& m, int&
 
 // cos / sin of every row's position for the fused epilogue (row = b * T + i,
 // position start_pos[b] + i); rows of an invalid sequence are left unset. Each
-// thread evaluates kQkvTabPer frequencies of one row, independent fp64 chains
-// that keep the fp64 pipe fed. The projection kernel is launched as this
-// kernel's programmatic dependent: it may start at once, and only its
-// epilogue waits for the table.
+// thread evaluates kQkvTabPer frequencies of one row at a time, independent
+// fp64 chains that keep the fp64 pipe fed, over a grid-stride loop. The
+// projection kernel is launched as this kernel's programmatic dependent: it may
+// start at once, and only its epilogue waits for the table. The table grid is
+// one small block per SM so that the projection's persistent CTAs fit beside
+// it (a grid sized to the work fills every SM's registers, and the projection
+// could then only start as the table drained).
 constexpr int kQkvTabPer = 4;
+constexpr int kQkvTabThreads = 128;
 
-__global__ void qkv_table_kernel(const int32_t* __restrict__ start_pos, int M, int T, int Tmax,
-                                 float* __restrict__ cos_tab, float* __restrict__ sin_tab, int32_t* status) {
+__global__ void __launch_bounds__(kQkvTabThreads) qkv_table_kernel(const int32_t* __restrict__ start_pos, int M,
+                                                                     int T, int Tmax, float* __restrict__ cos_tab,
+                                                                     float* __restrict__ sin_tab, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float s_inv[64];  // the 64 inverse frequencies, once per block (each is an fp64 power)
   if (threadIdx.x < 64) s_inv[threadIdx.x] = rope_inv_freq(threadIdx.x);
   __syncthreads();
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one (row, group of frequencies)
-  if (idx >= (long long)M * (64 / kQkvTabPer)) return;
-  const int row = int(idx / (64 / kQkvTabPer)), j0 = int(idx % (64 / kQkvTabPer)) * kQkvTabPer;
-  const int b = row / T, i = row % T;
-  const int s = __ldg(start_pos + b);
-  if (s < 0 || (long long)s + T > Tmax) {
-    if (i == 0 && j0 == 0) report(status, GROK_DEV_BAD_START);
-    return;
-  }
-  float c[kQkvTabPer], sn[kQkvTabPer];
+  const long long total = (long long)M * (64 / kQkvTabPer);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {   // one (row, group of frequencies)
+    const int row = int(idx / (64 / kQkvTabPer)), j0 = int(idx % (64 / kQkvTabPer)) * kQkvTabPer;
+    const int b = row / T, i = row % T;
+    const int s = __ldg(start_pos + b);
+    if (s < 0 || (long long)s + T > Tmax) {
+      if (i == 0 && j0 == 0) report(status, GROK_DEV_BAD_START);
+      continue;
+    }
+    float c[kQkvTabPer], sn[kQkvTabPer];
 #pragma unroll
-  for (int u = 0; u < kQkvTabPer; ++u) rope_cos_sin(__fmul_rn(float(s + i), s_inv[j0 + u]), c[u], sn[u]);
-  float4* cp = reinterpret_cast<float4*>(cos_tab + (size_t)row * 64 + j0);
-  float4* sp = reinterpret_cast<float4*>(sin_tab + (size_t)row * 64 + j0);
-  *cp = make_float4(c[0], c[1], c[2], c[3]);
-  *sp = make_float4(sn[0], sn[1], sn[2], sn[3]);
+    for (int u = 0; u < kQkvTabPer; ++u) rope_cos_sin(__fmul_rn(float(s + i), s_inv[j0 + u]), c[u], sn[u]);
+    float4* cp = reinterpret_cast<float4*>(cos_tab + (size_t)row * 64 + j0);
+    float4* sp = reinterpret_cast<float4*>(sin_tab + (size_t)row * 64 + j0);
+    *cp = make_float4(c[0], c[1], c[2], c[3]);
+    *sp = make_float4(sn[0], sn[1], sn[2], sn[3]);
+  }
 }
 
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
@@ -500,8 +507,23 @@ static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w
   prm.cache_v = reinterpret_cast<uint4*>(cache_v);
   prm.pm = pm;
   prm.status = dev_status;
+  int sms = 0;
+  grok_status st0 = device_sm_count(&sms);
+  if (st0 != GROK_OK) return st0;
   const long long total = M * (64 / kQkvTabPer);
-  qkv_table_kernel<<<unsigned((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  const long long want = (total + kQkvTabThreads - 1) / kQkvTabThreads;
+  const unsigned tab_grid = unsigned(want < sms ? want : sms);
+  // An SM's shared-memory / L1 split is set for the blocks it runs: with the
+  // default split for this small-smem kernel, the projection's CTAs could not
+  // join its SMs before the table blocks finished.
+  static bool tab_attr_set = false;  // idempotent: every thread would set the same value
+  if (!tab_attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(qkv_table_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         int(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    tab_attr_set = true;
+  }
+  qkv_table_kernel<<<tab_grid, kQkvTabThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       start_pos, int(M), T, Tmax, const_cast<float*>(prm.cos_tab), const_cast<float*>(prm.sin_tab), dev_status);
   grok_status st = check_launch("qkv table");
   if (st != GROK_OK) return st;
