@@ -56,6 +56,7 @@ EXPORTS = (
     "grok_attn_prefill_paged",
     "grok_attn_decode_paged",
     "grok_qkv_rope_append_paged",
+    "grok_kv_insert_slot",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -126,6 +127,8 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_decode_paged.argtypes = [P, P, P, I, P, I, P, I, P, S, P, P]
     lib.grok_qkv_rope_append_paged.restype = I
     lib.grok_qkv_rope_append_paged.argtypes = [P, P, P, I, I, P, P, P, I, P, I, P, S, P, P]
+    lib.grok_kv_insert_slot.restype = I
+    lib.grok_kv_insert_slot.argtypes = [P, P, I, I, I, P, P, I, I, P, I, P]
     _lib = lib
     return lib
 
@@ -479,3 +482,21 @@ def qkv_rope_append_paged(x, w, start_pos, q_rot, k_pool, v_pool, block_table, w
     _check(load().grok_qkv_rope_append_paged(_ptr(x), _ptr(w), _ptr(start_pos), B, T, _ptr(q_rot), _ptr(k_pool),
                                              _ptr(v_pool), n_pages, _ptr(block_table), max_pages, _ptr(workspace),
                                              nbytes, _ptr(dev_status), _stream(stream)))
+
+
+def kv_insert_slot(cache_k, cache_v, slot: int, src_k, src_v, n_rows: int, step=None, step_value: int = 0,
+                   stream=None) -> None:
+    """Continuous batching: rows [0, n_rows) of one sequence's caches [L, 8, 128] into batch slot `slot`.
+
+    step (int32 [B], optional) gets step[slot] = step_value.
+    """
+    B, Tmax = cache_k.shape[0], cache_k.shape[1]
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    L = src_k.shape[0]
+    _want(src_k, "src_k", torch.bfloat16, (L, N_KV_HEADS, HEAD_DIM))
+    _want(src_v, "src_v", torch.bfloat16, (L, N_KV_HEADS, HEAD_DIM))
+    if step is not None:
+        _want(step, "step", torch.int32, (B,))
+    _check(load().grok_kv_insert_slot(_ptr(cache_k), _ptr(cache_v), B, Tmax, int(slot), _ptr(src_k), _ptr(src_v), L,
+                                      int(n_rows), _ptr(step), int(step_value), _stream(stream)))

@@ -351,6 +351,29 @@ grok_status grok_qkv_rope_append_paged(const grok_bf16* x, const grok_bf16* w, c
                                        const int32_t* block_table, int max_pages, void* workspace, size_t ws_bytes,
                                        int32_t* dev_status, void* stream);
 
+/*
+ * Continuous-batching slot insertion (code-reading guide ch. 6 §6.6.1: every
+ * sequence has its own step, so a finished sequence's batch slot can be handed
+ * to a new request; the runner inserts the new sequence's memory into slot i
+ * along the batch axis, for the k and v caches and the step).
+ *
+ * grok_kv_insert_slot copies rows [0, n_rows) of one sequence's caches src_k,
+ * src_v [src_rows, 8, 128] into rows [0, n_rows) of slot `slot` of the batch
+ * caches cache_k, cache_v [B, Tmax, 8, 128] (all bf16, device, 16-byte
+ * aligned, caller-owned), and sets step[slot] = step_value when step (device
+ * int32 [B], e.g. the start_pos / kv_len array of the next call) is not NULL.
+ * Rows >= n_rows of the slot are left as they are: attention never reads rows
+ * at or beyond a sequence's step, so n_rows >= step_value gives the results of
+ * replacing the whole slot. The source rows must not overlap the slot.
+ * Argument errors return GROK_ERR_INVALID_ARG with nothing launched; one kernel
+ * launch otherwise (none when n_rows == 0 and step is NULL).
+ * With a paged cache (GROK_PAGE_TOKENS) no copy is needed: the new sequence's
+ * pages are named in its row of the block table.
+ */
+grok_status grok_kv_insert_slot(grok_bf16* cache_k, grok_bf16* cache_v, int B, int Tmax, int slot,
+                                const grok_bf16* src_k, const grok_bf16* src_v, int src_rows, int n_rows,
+                                int32_t* step, int step_value, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
