@@ -57,6 +57,8 @@ EXPORTS = (
     "grok_attn_decode_paged",
     "grok_qkv_rope_append_paged",
     "grok_kv_insert_slot",
+    "grok_attn_decode_step_workspace",
+    "grok_attn_decode_step",
 )
 
 _lib: Optional[ctypes.CDLL] = None
@@ -129,6 +131,10 @@ def load() -> ctypes.CDLL:
     lib.grok_qkv_rope_append_paged.argtypes = [P, P, P, I, I, P, P, P, I, P, I, P, S, P, P]
     lib.grok_kv_insert_slot.restype = I
     lib.grok_kv_insert_slot.argtypes = [P, P, I, I, I, P, P, I, I, P, I, P]
+    lib.grok_attn_decode_step_workspace.restype = I
+    lib.grok_attn_decode_step_workspace.argtypes = [I, I, ctypes.POINTER(S)]
+    lib.grok_attn_decode_step.restype = I
+    lib.grok_attn_decode_step.argtypes = [P, P, P, P, I, I, P, P, P, S, P, P, P]
     _lib = lib
     return lib
 
@@ -500,3 +506,39 @@ def kv_insert_slot(cache_k, cache_v, slot: int, src_k, src_v, n_rows: int, step=
         _want(step, "step", torch.int32, (B,))
     _check(load().grok_kv_insert_slot(_ptr(cache_k), _ptr(cache_v), B, Tmax, int(slot), _ptr(src_k), _ptr(src_v), L,
                                       int(n_rows), _ptr(step), int(step_value), _stream(stream)))
+
+
+
+def decode_step_workspace(B: int, Tmax: int) -> int:
+    """Bytes of workspace decode_step_chained() needs (q_rot and the split partials)."""
+    n = ctypes.c_size_t(0)
+    _check(load().grok_attn_decode_step_workspace(B, Tmax, ctypes.byref(n)))
+    return n.value
+
+
+def alloc_decode_step_workspace(B: int, Tmax: int, device=None) -> torch.Tensor:
+    return torch.empty(decode_step_workspace(B, Tmax), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_step_chained(q, k, v, start_pos, cache_k, cache_v, workspace, out, dev_status=None, stream=None) -> None:
+    """One decode step in one call: append the new token at start_pos, then attend over rows [0, start_pos].
+
+    q [B, 48, 128] (or [B, 1, 48, 128]), k, v [B, 8, 128] (or [B, 1, 8, 128]); the three kernels run as a
+    chain of programmatic dependents (see grok_attn_decode_step).
+    """
+    B, Tmax = cache_k.shape[0], cache_k.shape[1]
+    _want(q.view(B, N_Q_HEADS, HEAD_DIM), "q", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    _want(k.view(B, N_KV_HEADS, HEAD_DIM), "k", torch.bfloat16, (B, N_KV_HEADS, HEAD_DIM))
+    _want(v.view(B, N_KV_HEADS, HEAD_DIM), "v", torch.bfloat16, (B, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(out, "out", torch.bfloat16, (B, N_Q_HEADS, HEAD_DIM))
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().grok_attn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), B, Tmax, _ptr(cache_k),
+                                        _ptr(cache_v), _ptr(workspace), nbytes, _ptr(out), _ptr(dev_status),
+                                        _stream(stream)))

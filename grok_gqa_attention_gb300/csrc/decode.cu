@@ -55,8 +55,9 @@ __host__ __device__ inline DecWs dec_ws(void* base, int B, int n_split) {
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v,
                                                              const uint32_t* __restrict__ q_rot,
-                                                             const int32_t* __restrict__ kv_len, int Tmax,
-                                                             int n_split, DecWs ws, PageMap pm, int32_t* status) {
+                                                             const int32_t* __restrict__ kv_len, int kv_add,
+                                                             int Tmax, int n_split, DecWs ws, PageMap pm,
+                                                             int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes);
@@ -64,10 +65,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   int* abort_flag = reinterpret_cast<int*>(empty + kDecStages);
   volatile int* abort = abort_flag;
 
+  // A dependent combine may be scheduled as soon as every CTA has started.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = __ldg(kv_len + b);
-  if (L < 1 || L > Tmax) {
+  const long long L_ = (long long)__ldg(kv_len + b) + kv_add;
+  const int L = L_ < 1 || L_ > Tmax ? 0 : int(L_);
+  if (L < 1) {
     if (split == 0 && g == 0 && tid == 0) report(status, GROK_DEV_BAD_KV_LEN);
     return;
   }
@@ -83,18 +87,30 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     }
     *abort_flag = 0;
     fence_barrier_init();
-    for (int s = 0; s < kDecStages && s < n_st; ++s) {
-      uint8_t* base = smem + s * kDecStageBytes;
-      const int key0 = k0 + s * kDecKeysPerStage;
-      int row, bc;
-      kv_coord(pm, b, key0, row, bc, status);  // a 64-key tile never straddles a page
-      mbar_arrive_expect_tx(&full[s], kDecStageBytes);
-      tma_load_4d(base, &tm_k, &full[s], 0, g, row, bc);
-      tma_load_4d(base + kDecBox, &tm_k, &full[s], 64, g, row, bc);
-      tma_load_4d(base + 2 * kDecBox, &tm_v, &full[s], 0, g, row, bc);
-      tma_load_4d(base + 3 * kDecBox, &tm_v, &full[s], 64, g, row, bc);
-    }
   }
+  // The first stages of the ring. When this grid is the programmatic dependent
+  // of the append that wrote the newest row (kv_add = 1: rows < L - 1 are older
+  // than that grid and complete), the stages that cannot hold row L - 1 are
+  // loaded before waiting for it; the rest, q_rot included, after.
+  auto load_stage = [&](int s) {
+    uint8_t* base = smem + s * kDecStageBytes;
+    const int key0 = k0 + s * kDecKeysPerStage;
+    int row, bc;
+    kv_coord(pm, b, key0, row, bc, status);  // a 64-key tile never straddles a page
+    mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+    tma_load_4d(base, &tm_k, &full[s], 0, g, row, bc);
+    tma_load_4d(base + kDecBox, &tm_k, &full[s], 64, g, row, bc);
+    tma_load_4d(base + 2 * kDecBox, &tm_v, &full[s], 0, g, row, bc);
+    tma_load_4d(base + 3 * kDecBox, &tm_v, &full[s], 64, g, row, bc);
+  };
+  auto early = [&](int s) { return kv_add == 1 && k0 + (s + 1) * kDecKeysPerStage <= L - 1; };
+  if (tid == 0)
+    for (int s = 0; s < kDecStages && s < n_st; ++s)
+      if (early(s)) load_stage(s);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // no-op unless launched as a dependent
+  if (tid == 0)
+    for (int s = 0; s < kDecStages && s < n_st; ++s)
+      if (!early(s)) load_stage(s);
 
   // Q of the group's 6 heads as the A operand (rows lane/4; rows >= 6 and the
   // upper 8 rows are zero). A fragment: a0 = (row, k 2t..2t+1), a2 = (row, k 2t+8..).
@@ -233,11 +249,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 }
 
 __global__ void __launch_bounds__(192) combine_kernel(const DecWs ws, const int32_t* __restrict__ kv_len,
-                                                      int Tmax, int n_split, uint2* __restrict__ out,
+                                                      int kv_add, int Tmax, int n_split, uint2* __restrict__ out,
                                                       int32_t* status) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials of a decode grid this one depends on
   const int g = blockIdx.x, b = blockIdx.y;
-  const int L = __ldg(kv_len + b);
-  if (L < 1 || L > Tmax) {
+  const long long L_ = (long long)__ldg(kv_len + b) + kv_add;
+  const int L = L_ < 1 || L_ > Tmax ? 0 : int(L_);
+  if (L < 1) {
     if (g == 0 && threadIdx.x == 0) report(status, GROK_DEV_BAD_KV_LEN);
     return;
   }
@@ -289,9 +307,12 @@ static grok_status decode_args(const void* ws, size_t ws_bytes, const int32_t* k
   return GROK_OK;
 }
 
+// pdl: launch as the programmatic dependent of the kernel before it on the
+// stream (the decode step's append); kv_add: kv_len[b] + kv_add keys.
 static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
-                                 uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* kv_len, int B,
-                                 int Tmax, void* workspace, int32_t* dev_status, void* stream) {
+                                 uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* kv_len, int kv_add,
+                                 int B, int Tmax, void* workspace, int32_t* dev_status, void* stream,
+                                 bool pdl = false) {
   grok_status st;
   int sms = 0;
   if ((st = device_sm_count(&sms)) != GROK_OK) return st;
@@ -308,10 +329,39 @@ static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src,
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set = true;
   }
-  const dim3 grid(ns, kKVHeads, B);
-  decode_kernel<<<grid, kDecThreads, kDecSmem, static_cast<cudaStream_t>(stream)>>>(
-      tk, tv, reinterpret_cast<const uint32_t*>(q_rot), kv_len, Tmax, ns, dec_ws(workspace, B, ns), pm, dev_status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ns, kKVHeads, B);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, tk, tv, reinterpret_cast<const uint32_t*>(q_rot), kv_len,
+                                     kv_add, Tmax, ns, dec_ws(workspace, B, ns), pm, dev_status);
+  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return check_launch("decode");
+}
+
+static grok_status combine_launch(const void* workspace, const int32_t* kv_len, int kv_add, int B, int Tmax,
+                                  grok_bf16* out, int32_t* dev_status, void* stream, bool pdl = false) {
+  const int ns = (Tmax + kDecSplit - 1) / kDecSplit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kKVHeads, B);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, dec_ws(const_cast<void*>(workspace), B, ns), kv_len,
+                                     kv_add, Tmax, ns, reinterpret_cast<uint2*>(out), dev_status);
+  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+  return check_launch("combine");
 }
 
 extern "C" grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k,
@@ -323,8 +373,8 @@ extern "C" grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16*
     return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode: bf16 tensors must be 16-byte aligned");
   grok_status st = decode_args(workspace, workspace_bytes, kv_len, B, Tmax, "grok_attn_decode");
   if (st != GROK_OK) return st;
-  return decode_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, kv_len, B, Tmax,
-                       workspace, dev_status, stream);
+  return decode_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, kv_len, 0, B,
+                       Tmax, workspace, dev_status, stream);
 }
 
 extern "C" grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok_bf16* k_pool,
@@ -345,7 +395,8 @@ extern "C" grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok
   grok_status st = decode_args(workspace, workspace_bytes, kv_len, B, int(Tmax), "grok_attn_decode_paged");
   if (st != GROK_OK) return st;
   return decode_launch(q_rot, k_pool, v_pool, uint64_t(n_pages) * GROK_PAGE_TOKENS, 1,
-                       PageMap{block_table, max_pages, n_pages}, kv_len, B, int(Tmax), workspace, dev_status, stream);
+                       PageMap{block_table, max_pages, n_pages}, kv_len, 0, B, int(Tmax), workspace, dev_status,
+                       stream);
 }
 
 extern "C" grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len,
@@ -356,10 +407,7 @@ extern "C" grok_status grok_attn_combine(const void* workspace, size_t workspace
   if (st != GROK_OK) return st;
   int sms = 0;
   if ((st = device_sm_count(&sms)) != GROK_OK) return st;
-  const int ns = (Tmax + kDecSplit - 1) / kDecSplit;
-  combine_kernel<<<dim3(kKVHeads, B), 192, 0, static_cast<cudaStream_t>(stream)>>>(
-      dec_ws(const_cast<void*>(workspace), B, ns), kv_len, Tmax, ns, reinterpret_cast<uint2*>(out), dev_status);
-  return check_launch("combine");
+  return combine_launch(workspace, kv_len, 0, B, Tmax, out, dev_status, stream);
 }
 
 // ----------------------------------------------------------------------------
@@ -422,4 +470,49 @@ extern "C" grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, cons
   if ((st = grok_attn_decode(q_rot, cache_k, cache_v, kv_len, B, Tmax, ws, need, dev_status, stream)) != GROK_OK)
     return st;
   return grok_attn_combine(ws, need, kv_len, B, Tmax, out, dev_status, stream);
+}
+
+// ----------------------------------------------------------------------------
+// One whole decode step as a chain of programmatic dependents: append (the new
+// token's RoPE and cache write), split-K decode, combine. Each kernel may start
+// while the one before it finishes; the decode loads the cache stages that
+// cannot hold the new row before it waits for the append, the combine waits
+// for the decode. The append is launched normally, so everything written on the
+// stream before the call (the caches, start_pos) is complete when the decode
+// starts.
+static size_t step_q_bytes(int B) { return (size_t(B) * kQHeads * kD * sizeof(grok_bf16) + 255) & ~size_t(255); }
+
+extern "C" grok_status grok_attn_decode_step_workspace(int B, int Tmax, size_t* bytes) {
+  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step_workspace: null pointer");
+  if (B < 1 || Tmax < 1 || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step_workspace: need B >= 1, 1 <= Tmax <= %d",
+                GROK_MAX_POSITION);
+  *bytes = step_q_bytes(B) + dec_ws_bytes(B, (Tmax + kDecSplit - 1) / kDecSplit);
+  return GROK_OK;
+}
+
+extern "C" grok_status grok_attn_decode_step(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                             const int32_t* start_pos, int B, int Tmax, grok_bf16* cache_k,
+                                             grok_bf16* cache_v, void* workspace, size_t workspace_bytes,
+                                             grok_bf16* out, int32_t* dev_status, void* stream) {
+  if (!q || !k || !v || !start_pos || !cache_k || !cache_v || !workspace || !out)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step: null pointer");
+  if (!aligned16(out)) return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step: out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step: workspace must be 256-byte aligned");
+  size_t need = 0;
+  grok_status st = grok_attn_decode_step_workspace(B, Tmax, &need);
+  if (st != GROK_OK) return st;
+  if (workspace_bytes < need)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_decode_step: workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, need);
+  grok_bf16* q_rot = static_cast<grok_bf16*>(workspace);
+  void* dws = static_cast<char*>(workspace) + step_q_bytes(B);
+  if ((st = grok_rope_kv_append(q, k, v, start_pos, B, 1, Tmax, q_rot, cache_k, cache_v, dev_status, stream)) !=
+      GROK_OK)
+    return st;
+  if ((st = decode_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos, 1,
+                          B, Tmax, dws, dev_status, stream, true)) != GROK_OK)
+    return st;
+  return combine_launch(dws, start_pos, 1, B, Tmax, out, dev_status, stream, true);
 }

@@ -62,6 +62,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int32_t* __restrict__ start_pos, int B, int T, int Tmax, uint4* __restrict__ q_rot,
     uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, PageMap pm, int32_t* status) {
+  // A kernel launched as this grid's programmatic dependent (the decode step's
+  // split-K decode) may start at once; it waits for this grid before reading
+  // what it writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float s_inv[64];
   __shared__ float s_cos[kRopeWarps][64];
   __shared__ float s_sin[kRopeWarps][64];
@@ -173,6 +177,17 @@ static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const g
                : team == 4 ? rope_kv_append_kernel<4>
                : team == 2 ? rope_kv_append_kernel<2>
                            : rope_kv_append_kernel<1>;
+  // Few tokens (a decode step): the SMs' shared-memory split is set for the
+  // decode kernel that may join them, not for this kernel's 2 KB.
+  static bool carve_set = false;  // idempotent: every thread would set the same values
+  if (!carve_set) {
+    for (auto kf : {rope_kv_append_kernel<8>, rope_kv_append_kernel<4>, rope_kv_append_kernel<2>}) {
+      cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           int(cudaSharedmemCarveoutMaxShared));
+      if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    }
+    carve_set = true;
+  }
   kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
       start_pos, B, T, Tmax, reinterpret_cast<uint4*>(q_rot), reinterpret_cast<uint4*>(cache_k),

@@ -199,6 +199,28 @@ grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16
                                          int32_t* dev_status, void* stream);
 
 /*
+ * One whole decode step in one call (ch. 4 §4.4 and §4.4.1: the new token's
+ * K and V are rotated and written into the cache at step[b], then attention
+ * over rows [0, step[b]] with the memory mask):
+ *   grok_rope_kv_append(q, k, v, start_pos, B, T = 1, Tmax, ...), then
+ *   grok_attn_decode and grok_attn_combine with kv_len[b] = start_pos[b] + 1.
+ * Same bits as those three calls. The decode and combine are launched as
+ * programmatic dependents of the kernel before them: each may start while its
+ * predecessor finishes, and the decode loads the cache rows the append does
+ * not write before it waits for the append.
+ *   q [B,48,128], k, v [B,8,128] bf16; start_pos [B] int32 (the new token's
+ *   position, 0 <= start_pos[b] < Tmax); cache_k, cache_v [B,Tmax,8,128];
+ *   out [B,48,128] bf16. workspace: caller-owned device memory, 256-byte
+ *   aligned, of at least grok_attn_decode_step_workspace(B, Tmax) bytes (it
+ *   holds q_rot and the split partials). Errors as for the three calls.
+ */
+grok_status grok_attn_decode_step_workspace(int B, int Tmax, size_t* bytes);
+grok_status grok_attn_decode_step(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                  const int32_t* start_pos, int B, int Tmax, grok_bf16* cache_k, grok_bf16* cache_v,
+                                  void* workspace, size_t workspace_bytes, grok_bf16* out, int32_t* dev_status,
+                                  void* stream);
+
+/*
  * Q/K/V projection (code-reading guide ch. 4 §4.1 Linear, §4.5.1 Q/K/V
  * projection): the three bias-free Linears of the attention call as one
  * product with the weights side by side.
