@@ -15,6 +15,8 @@ namespace grok {
 grok_status fail(grok_status s, const char* fmt, ...);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Outputs written with 32-byte stores (st.global.v8.b32) need 32-byte alignment.
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // The current device must be compute capability 10.3; returns its SM count.
 grok_status device_sm_count(int* sm_count);

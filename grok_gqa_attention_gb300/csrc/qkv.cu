@@ -362,39 +362,52 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
 // Int8 weight-only quantisation (ch. 4 §4.1, §4.1.1 QuantizedWeight8bit): the
 // weight is int8 [K, N] with one fp32 scale per output column, dequantized as
 // an fp32 product rounded to fp32, then rounded to bf16 (the pages' order:
-// astype(scales.dtype) * scales, then astype(bf16)). Each thread converts 16
-// consecutive weights of one row: one 16-byte load, two 16-byte stores.
-__device__ __forceinline__ void dequant16(uint4 raw, const float4* __restrict__ scales, int n0, uint4* dst) {
+// astype(scales.dtype) * scales, then astype(bf16)).
+// Each thread owns one 16-column chunk of the weight (its 16 scales stay in
+// registers) and walks down the rows of its column, four rows per pass with
+// all four loads issued before any converts; each chunk's 16 bf16 go out as
+// one 32-byte store. Grid: (column blocks, row groups). Memory-bound: 1 byte
+// read and 2 written per weight.
+constexpr int kDqThreads = 128;
+constexpr int kDqRows = 4;
+
+__device__ __forceinline__ void dequant16r(uint4 raw, const float (&sc)[16], uint4* dst) {
   const uint32_t word[4] = {raw.x, raw.y, raw.z, raw.w};
   uint32_t out[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float4 sc = __ldg(scales + (n0 >> 2) + q);
-    const float sv[4] = {sc.x, sc.y, sc.z, sc.w};
     float f[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const int v = int(word[q] << (24 - 8 * b)) >> 24;  // sign-extended byte b
-      f[b] = __fmul_rn(float(v), sv[b]);
+      f[b] = __fmul_rn(float(v), sc[4 * q + b]);
     }
     out[2 * q] = pack_bf16x2(f[0], f[1]);
     out[2 * q + 1] = pack_bf16x2(f[2], f[3]);
   }
-  dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-  dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  st_global_v8(dst, out);  // one 32-byte store (w16 is 32-byte aligned)
 }
 
-// Two chunks per thread per pass, both loads issued before either converts.
-__global__ void dequant_int8_kernel(const uint4* __restrict__ w8, const float4* __restrict__ scales, long long chunks,
-                                    int N, uint4* __restrict__ w16) {
+__global__ void __launch_bounds__(kDqThreads) dequant_int8_kernel(const uint4* __restrict__ w8,
+                                                                  const float4* __restrict__ scales, int K, int N,
+                                                                  uint4* __restrict__ w16) {
   const int per_row = N / 16;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += 2 * stride) {
-    const long long c2 = c + stride;
-    const uint4 r1 = __ldg(w8 + c);
-    const uint4 r2 = c2 < chunks ? __ldg(w8 + c2) : make_uint4(0, 0, 0, 0);
-    dequant16(r1, scales, int(c % per_row) * 16, w16 + 2 * c);
-    if (c2 < chunks) dequant16(r2, scales, int(c2 % per_row) * 16, w16 + 2 * c2);
+  const int cc = blockIdx.x * kDqThreads + threadIdx.x;  // column chunk
+  if (cc >= per_row) return;
+  float sc[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = __ldg(scales + cc * 4 + q);
+    sc[4 * q] = v.x, sc[4 * q + 1] = v.y, sc[4 * q + 2] = v.z, sc[4 * q + 3] = v.w;
+  }
+  for (int r0 = blockIdx.y * kDqRows; r0 < K; r0 += gridDim.y * kDqRows) {
+    uint4 raw[kDqRows];
+#pragma unroll
+    for (int u = 0; u < kDqRows; ++u)
+      if (r0 + u < K) raw[u] = __ldg(w8 + (size_t)(r0 + u) * per_row + cc);
+#pragma unroll
+    for (int u = 0; u < kDqRows; ++u)
+      if (r0 + u < K) dequant16r(raw[u], sc, w16 + 2 * ((size_t)(r0 + u) * per_row + cc));
   }
 }
 
@@ -453,8 +466,8 @@ using namespace grok;
 extern "C" grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, int N, grok_bf16* y,
                                    int32_t* dev_status, void* stream) {
   if (!x || !w || !y) return fail(GROK_ERR_INVALID_ARG, "grok_linear: null pointer");
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y))
-    return fail(GROK_ERR_INVALID_ARG, "grok_linear: tensors must be 16-byte aligned");
+  if (!aligned16(x) || !aligned16(w) || !aligned32(y))
+    return fail(GROK_ERR_INVALID_ARG, "grok_linear: x and w must be 16-byte aligned, y 32-byte aligned");
   if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || N < kQkvBN || N % kQkvBN != 0)
     return fail(GROK_ERR_INVALID_ARG,
                 "grok_linear: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)", kQkvBK,
@@ -485,9 +498,10 @@ static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w
                                           void* stream, const char* name) {
   if (!x || !w || !start_pos || !q_rot || !cache_k || !cache_v || !workspace)
     return fail(GROK_ERR_INVALID_ARG, "%s: null pointer", name);
-  if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) ||
+  if (!aligned16(x) || !aligned16(w) || !aligned32(q_rot) || !aligned32(cache_k) || !aligned32(cache_v) ||
       !aligned16(workspace))
-    return fail(GROK_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
+    return fail(GROK_ERR_INVALID_ARG, "%s: x, w and the workspace must be 16-byte aligned, q_rot and the caches "
+                "32-byte aligned", name);
   if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
     return fail(GROK_ERR_INVALID_ARG, "%s: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)", name,
                 GROK_MAX_POSITION, B, T, Tmax);
@@ -557,19 +571,24 @@ extern "C" grok_status grok_qkv_rope_append_paged(const grok_bf16* x, const grok
 extern "C" grok_status grok_dequant_int8(const int8_t* w8, const float* scales, int K, int N, grok_bf16* w16,
                                          void* stream) {
   if (!w8 || !scales || !w16) return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: null pointer");
-  if (!aligned16(w8) || !aligned16(scales) || !aligned16(w16))
-    return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: tensors must be 16-byte aligned");
+  if (!aligned16(w8) || !aligned16(scales) || !aligned32(w16))
+    return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: w8 and scales must be 16-byte aligned, w16 32-byte aligned");
   if (K < 1 || N < 16 || N % 16 != 0)
     return fail(GROK_ERR_INVALID_ARG, "grok_dequant_int8: need K >= 1 and N a positive multiple of 16 (K=%d N=%d)", K,
                 N);
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
-  const long long chunks = (long long)K * N / 16;
-  long long blocks = (chunks + 255) / 256;
-  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-  dequant_int8_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4*>(w8), reinterpret_cast<const float4*>(scales), chunks, N,
+  const int per_row = N / 16;
+  const int col_blocks = (per_row + kDqThreads - 1) / kDqThreads;
+  // about 16 resident blocks of kDqThreads per SM in total, each walking its rows
+  long long row_groups = ((long long)sms * 16 + col_blocks - 1) / col_blocks;
+  const long long max_groups = ((long long)K + kDqRows - 1) / kDqRows;
+  if (row_groups > max_groups) row_groups = max_groups;
+  if (row_groups > 65535) row_groups = 65535;
+  dequant_int8_kernel<<<dim3(unsigned(col_blocks), unsigned(row_groups)), kDqThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(w8), reinterpret_cast<const float4*>(scales), K, N,
       reinterpret_cast<uint4*>(w16));
   return check_launch("dequant_int8");
 }
@@ -585,6 +604,8 @@ extern "C" grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, co
                                         int N, grok_bf16* y, void* workspace, size_t ws_bytes, int32_t* dev_status,
                                         void* stream) {
   if (!workspace) return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: null workspace");
+  if (!aligned32(workspace) || !aligned32(y))
+    return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: the workspace and y must be 32-byte aligned");
   if (ws_bytes < size_t(K) * N * sizeof(grok_bf16))
     return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: workspace of %zu bytes, need %zu", ws_bytes,
                 size_t(K) * N * sizeof(grok_bf16));

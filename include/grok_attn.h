@@ -21,7 +21,9 @@
  *       cache_k/v      [B, Tmax, 8, 128]
  *   - every pointer argument is a DEVICE pointer owned by the caller; the
  *     library never allocates, frees or retains caller memory, and every
- *     pointer to a bf16 tensor must be 16-byte aligned.
+ *     pointer to a bf16 tensor must be 16-byte aligned (32-byte for the outputs
+ *     of the projection, Linear and dequant calls below, which are written with
+ *     32-byte stores).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every call
  *     is asynchronous on it and returns after enqueueing its kernels.
  *   - errors found on the host (null or misaligned pointers, bad sizes) return
@@ -238,7 +240,8 @@ grok_status grok_attn_decode_step(const grok_bf16* q, const grok_bf16* k, const 
  *   grok_qkv_workspace(B, T) bytes (a per-step cos/sin table), 16-byte aligned.
  *   A sequence whose start_pos[b] + T > Tmax (or start < 0) sets
  *   GROK_DEV_BAD_START and none of its rows are written.
- * All pointers device-resident, 16-byte aligned; work is asynchronous on stream.
+ * All pointers device-resident and 16-byte aligned; the outputs (y; q_rot,
+ * cache_k, cache_v) 32-byte aligned. Work is asynchronous on stream.
  */
 grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok_bf16* y, int32_t* dev_status,
                              void* stream);
@@ -246,8 +249,8 @@ grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok
 /*
  * A bias-free Linear (ch. 4 §4.1) on the same tensor-core kernel:
  * y [M, N] = x [M, K] . w [K, N], bf16, fp32 accumulation, one rounding.
- * K must be a positive multiple of 64 and N of 256; 1 <= M <= 2^30. Row-major,
- * 16-byte aligned device tensors. Serves the output projection (ch. 4 §4.5.4:
+ * K must be a positive multiple of 64 and N of 256; 1 <= M <= 2^30. Row-major
+ * device tensors, x and w 16-byte aligned, y 32-byte aligned. Serves the output projection (ch. 4 §4.5.4:
  * attention output [B*T, 48*128] head-major . W_o [6144, 6144]) and each
  * tensor-parallel rank's share of it (the rows of W_o for the rank's heads,
  * K = 6144 / ranks; the ranks' partial outputs are summed by the caller).
@@ -269,7 +272,8 @@ grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, in
  *   grok_linear (so K % 64 == 0, N % 256 == 0). For prefill-sized M the
  *   product is tensor-bound and the one pass over the weight costs a few
  *   percent; the workspace may be reused across calls with the same weight.
- * All pointers device-resident and 16-byte aligned; asynchronous on stream.
+ * All pointers device-resident and 16-byte aligned; w16, the workspace and y
+ * 32-byte aligned. Asynchronous on stream.
  */
 grok_status grok_dequant_int8(const int8_t* w8, const float* scales, int K, int N, grok_bf16* w16, void* stream);
 grok_status grok_linear_int8_workspace(int K, int N, size_t* bytes);
@@ -351,7 +355,8 @@ grok_status grok_prefill_pipe_destroy(grok_prefill_pipe* pipe);
  *   * GROK_PAGE_TOKENS, ...).
  * grok_qkv_rope_append_paged: grok_qkv_rope_append (the projection fused with
  *   RoPE and the append) writing the k and v rows through the table; the
- *   workspace is sized by grok_qkv_workspace(B, T).
+ *   workspace is sized by grok_qkv_workspace(B, T); q_rot and the pools must
+ *   be 32-byte aligned, as for grok_qkv_rope_append.
  * Argument errors (null pointers, misaligned tensors, n_pages < 1,
  * max_pages < 1, sizes past the limits above) return GROK_ERR_INVALID_ARG with
  * nothing launched.

@@ -221,3 +221,21 @@ def test_linear_int8_matches_oracle():
     _projection_check(W.bits(y.cpu()), P.linear_exact(W.bits(x), w16), "int8 linear", K=K)
     with pytest.raises(G.GrokError):   # workspace too small
         G.linear_int8(x.cuda(), w8.cuda(), scales.cuda(), y, ws[:16])
+
+
+def test_outputs_written_with_32_byte_stores_must_be_32_byte_aligned():
+    """A 16-byte aligned but not 32-byte aligned output is rejected on the host (nothing is launched)."""
+    x = torch.zeros((256, 6144), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((6144, 8192), dtype=torch.bfloat16, device="cuda")
+    buf = torch.zeros(256 * 8192 + 16, dtype=torch.bfloat16, device="cuda")
+    y_off = buf[8:8 + 256 * 8192].view(256, 8192)          # base + 16 bytes
+    assert y_off.data_ptr() % 32 == 16
+    with pytest.raises(G.GrokError):
+        G.qkv_project(x, w, y_off)
+    w8 = torch.zeros((64, 256), dtype=torch.int8, device="cuda")
+    sc = torch.ones(256, dtype=torch.float32, device="cuda")
+    wbuf = torch.zeros(64 * 256 + 16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(G.GrokError):
+        G.dequant_int8(w8, sc, wbuf[8:8 + 64 * 256].view(64, 256))
+    G.dequant_int8(w8, sc, wbuf[16:16 + 64 * 256].view(64, 256))   # 32-byte aligned offset: accepted
+    torch.cuda.synchronize()
