@@ -17,16 +17,22 @@
 // tensor-parallel rank's head slice of it.
 //
 // Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0      TMA producer: per 64-wide K block one X box [128 rows x 64] and
-//               four W boxes [64 rows x 64 columns] into a 4-stage ring
+//   warp 0      TMA producer: per 64-wide K block two X boxes [128 rows x 64]
+//               and four W boxes [64 rows x 64 columns] (64 KB) into a 3-stage
+//               ring
 //   warp 1      TMEM owner and MMA issuer (converged; one fixed lane issues)
 //   warps 2-5   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
 //               row per thread
-// Tile = 128 rows x 256 columns (two heads); tcgen05.mma M=128, N=256, K=16,
-// A = X (K-major), B = W (N-contiguous rows, MN-major), both 128-byte
-// swizzled. Two 256-column TMEM accumulators: the epilogue of one tile
-// overlaps the products of the next. Tiles go in groups of eight 128-row
-// blocks by all 32 column blocks, so the tiles in flight share X and W in L2.
+// Tile = 256 rows x 256 columns (two heads), as two 128-row halves that share
+// each staged W block: tcgen05.mma M=128, N=256, K=16 per half, A = X
+// (K-major), B = W (N-contiguous rows, MN-major), both 128-byte swizzled. The
+// halves accumulate in TMEM columns 0..255 and 256..511. Sharing W between the
+// halves is what keeps the MMAs fed: a 128-row tile needs 48 KB per 512 MMA
+// cycles from L2 (94 B/cycle per SM), more than an SM's TMA stream delivers,
+// the 256-row tile 64 KB per 1024 cycles. The epilogue drains half 0 while
+// half 1's last products run, and the next tile's half-0 products start while
+// half 1 is drained. Tiles go in groups of eight 256-row blocks by all the
+// column blocks, so the tiles in flight share X and W in L2.
 //
 // Epilogues: plain (write Y) or fused (q heads: RoPE -> q_rot; k heads: RoPE
 // -> cache_k at row start_pos[b] + i, or at its page of a paged pool; v heads
@@ -44,14 +50,16 @@ namespace grok {
 
 constexpr int kQkvK = 6144;                 // model size
 constexpr int kQkvN = 8192;                 // 48 * 128 + 2 * 8 * 128
-constexpr int kQkvBM = 128, kQkvBN = 256, kQkvBK = 64;
-constexpr int kQkvStages = 4;
+constexpr int kQkvBM = 256, kQkvBN = 256, kQkvBK = 64;  // tile: two 128-row MMA halves
+constexpr int kQkvHM = 128;                               // rows per MMA and per X box
+constexpr int kQkvStages = 3;
 constexpr int kQkvThreads = 192;
 constexpr int kQkvGroupM = 8;
-constexpr int kQkvABytes = kQkvBM * kQkvBK * 2;             // 16 KB
+constexpr int kQkvABox = kQkvHM * kQkvBK * 2;               // 16 KB: one half's X block
+constexpr int kQkvABytes = 2 * kQkvABox;                    // 32 KB
 constexpr int kQkvBBox = kQkvBK * 64 * 2;                   // 8 KB: 64 K rows x 64 columns
 constexpr int kQkvBBytes = 4 * kQkvBBox;                    // 32 KB
-constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;     // 48 KB
+constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;     // 64 KB
 
 struct QkvBars {
   uint64_t full[kQkvStages], empty[kQkvStages];
@@ -205,6 +213,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           uint8_t* sa = smem + st * kQkvStageBytes;
           mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
           tma_load_4d(sa, &tm_x, &bars->full[st], kb * kQkvBK, m * kQkvBM, 0, 0);
+          tma_load_4d(sa + kQkvABox, &tm_x, &bars->full[st], kb * kQkvBK, m * kQkvBM + kQkvHM, 0, 0);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tma_load_4d(sa + kQkvABytes + c * kQkvBBox, &tm_w, &bars->full[st], n * kQkvBN + c * 64, kb * kQkvBK, 0, 0);
@@ -218,14 +227,16 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one();
-    constexpr uint32_t idesc = make_idesc_bf16(kQkvBM, kQkvBN, 1);
+    constexpr uint32_t idesc = make_idesc_bf16(kQkvHM, kQkvBN, 1);
     int it = 0, tc = 0;
     bool ok = true;
+    // TMEM: half 0 of the tile accumulates in columns 0..255, half 1 in 256..511.
+    // The epilogue drains half 0 first: the next tile's half-0 products start
+    // while half 1 is still being read out.
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tc) {
-      const int ab = tc & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[ab], ((tc >> 1) & 1) ^ 1, abort, p.status))) break;
+      const uint32_t par = uint32_t(tc & 1) ^ 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[0], par, abort, p.status))) break;
       tc_fence_after();
-      const uint32_t d = tmem + ab * kQkvBN;
       for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
         const int st = it % kQkvStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[st], (it / kQkvStages) & 1, abort, p.status))) {
@@ -233,20 +244,36 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           break;
         }
         tc_fence_after();
+        const uint32_t sa = smem_u32(smem + st * kQkvStageBytes);
+        const uint64_t bdesc = make_sdesc_sw128(sa + kQkvABytes, kQkvBBox, 1024);
         if (leader) {
-          const uint32_t sa = smem_u32(smem + st * kQkvStageBytes);
           const uint64_t adesc = make_sdesc_sw128(sa, 16, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(sa + kQkvABytes, kQkvBBox, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 64 in steps of 16: A +32 B, B +16 rows (2048 B)
-            umma_ss(d, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
+            umma_ss(tmem, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
+                    (kb > 0 || kk > 0) ? 1u : 0u);
+          if (kb == p.k_blocks - 1) umma_commit(&bars->acc_full[0]);
+        }
+        __syncwarp();
+        if (kb == 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[1], par, abort, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (leader) {
+          const uint64_t adesc = make_sdesc_sw128(sa + kQkvABox, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ss(tmem + kQkvBN, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
                     (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars->empty[st]);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (leader) umma_commit(&bars->acc_full[ab]);
+      if (leader) umma_commit(&bars->acc_full[1]);
       __syncwarp();
     }
     // No MMA may still be running when TMEM is released.
@@ -266,12 +293,16 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tc) {
       int m, n;
       qkv_tile(p, t, m, n);
-      const int ab = tc & 1;
-      const bool ok = mbar_wait(&bars->acc_full[ab], (tc >> 1) & 1, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      bool ok_all = true;
+      for (int hf = 0; hf < 2; ++hf) {   // the tile's two 128-row halves, half 0 first
+      const bool ok = mbar_wait(&bars->acc_full[hf], tc & 1, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok_all = false;
+        break;
+      }
       tc_fence_after();
-      const uint32_t acc = tmem + tlane + ab * kQkvBN;
-      const int row = m * kQkvBM + r;
+      const uint32_t acc = tmem + tlane + hf * kQkvBN;
+      const int row = m * kQkvBM + hf * kQkvHM + r;
       const bool live = row < p.M;
       if (!kFused) {
         uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * p.N + n * kQkvBN) * 2;
@@ -346,7 +377,9 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->acc_empty[ab]);
+      mbar_arrive(&bars->acc_empty[hf]);
+      }
+      if (!ok_all) break;
     }
   }
 
@@ -420,7 +453,7 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   {
     const uint64_t dims[4] = {uint64_t(K), uint64_t(M), 1, 1};
     const uint64_t strides[3] = {uint64_t(K) * 2, uint64_t(K) * 2 * M, uint64_t(K) * 2 * M};
-    const uint32_t box[4] = {uint32_t(kQkvBK), uint32_t(kQkvBM), 1, 1};
+    const uint32_t box[4] = {uint32_t(kQkvBK), uint32_t(kQkvHM), 1, 1};
     if ((st = encode_tmap_bf16_4d(&tx, x, dims, strides, box)) != GROK_OK) return st;
   }
   {
