@@ -68,3 +68,34 @@ def test_bad_sizes_rejected(lib):
     p = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check fails first
     assert lib.grok_rope_kv_append(p, p, p, p, 1, 9, 8, p, p, p, None, None) == 1   # T > Tmax
     assert lib.grok_attn_prefill(p, p, p, p, None, 0, 1, 1, p, None, None) == 1     # B = 0
+
+
+def test_decode_step_workspace_is_host_only(lib):
+    n = ctypes.c_size_t(0)
+    s = ctypes.c_int(0)
+    assert lib.grok_attn_decode_workspace(32, 8192, ctypes.byref(n), ctypes.byref(s)) == 0
+    dec = n.value
+    assert lib.grok_attn_decode_step_workspace(32, 8192, ctypes.byref(n)) == 0
+    q_rot = 32 * 48 * 128 * 2  # the step's q_rot, 256-byte aligned ahead of the split partials
+    assert n.value == ((q_rot + 255) // 256) * 256 + dec
+    assert lib.grok_attn_decode_step_workspace(0, 8192, ctypes.byref(n)) == 1
+    assert lib.grok_attn_decode_step_workspace(1, 70000, ctypes.byref(n)) == 1
+
+
+def test_new_entry_points_reject_null_pointers_before_any_device_call(lib):
+    N = None
+    # paged calls, slot insertion and the one-call decode step all check their pointers first
+    assert lib.grok_attn_decode_paged(N, N, N, 1, N, 1, N, 1, N, 0, N, N) == 1
+    assert lib.grok_attn_prefill_paged(N, N, N, 1, N, 1, N, N, 1, 1, N, N, N) == 1
+    assert lib.grok_rope_kv_append_paged(N, N, N, N, 1, 1, N, N, N, 1, N, 1, N, N) == 1
+    assert lib.grok_kv_insert_slot(N, N, 1, 1, 0, N, N, 1, 1, N, 0, N) == 1
+    assert lib.grok_attn_decode_step(N, N, N, N, 1, 1, N, N, N, 0, N, N, N) == 1
+    assert b"null" in lib.grok_last_error()
+
+
+def test_misaligned_outputs_rejected_before_any_device_call(lib):
+    a32 = ctypes.c_void_p(1 << 20)          # 32-byte aligned, never dereferenced
+    a16 = ctypes.c_void_p((1 << 20) + 16)   # 16- but not 32-byte aligned
+    assert lib.grok_linear(a32, a32, 256, 64, 256, a16, None, None) == 1
+    assert b"32-byte" in lib.grok_last_error()
+    assert lib.grok_dequant_int8(a32, a32, 64, 256, a16, None) == 1
