@@ -12,7 +12,21 @@
  *     §4.5.4         weighted sum of V, heads flattened in order h = 6 g + r
  *   ch. 6 "model.py close reading II"
  *     §6.4.2         causal (tril) x key-padding mask; decode masks through the memory mask
- *     §6.6 / §6.6.1  KVMemory(k, v, step): caches [B, Tmax, 8, 128] bf16, per-sequence step
+ *     §6.6 / §6.6.1  KVMemory(k, v, step): caches [B, Tmax, 8, 128] bf16, per-sequence step;
+ *                    continuous batching (a new request takes a finished sequence's slot)
+ *     §6.6.2         paged KV cache (pages allocated only when used)
+ *
+ * Calls by group:
+ *   attention core      grok_rope_kv_append, grok_rope_cos_sin, grok_attn_prefill,
+ *                       grok_attn_decode_workspace, grok_attn_decode, grok_attn_combine,
+ *                       grok_attn_decode_step_static, grok_attn_decode_step(_workspace)
+ *   projections         grok_qkv_project, grok_linear, grok_dequant_int8,
+ *                       grok_linear_int8(_workspace), grok_qkv_workspace, grok_qkv_rope_append
+ *   runtime             grok_prefill_pipe_create / _submit / _wait / _destroy
+ *   paged cache         grok_rope_kv_append_paged, grok_attn_prefill_paged,
+ *                       grok_attn_decode_paged, grok_qkv_rope_append_paged
+ *   continuous batching grok_kv_insert_slot
+ *   diagnostics         grok_abi_version, grok_last_error, grok_selftest_bounded_wait
  *
  * Conventions for every call:
  *   - bf16 tensors are passed as grok_bf16 (uint16_t storage), row-major with the
