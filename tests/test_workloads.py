@@ -1,5 +1,6 @@
 """The seeded input generator: shapes, determinism and the junk fill of unused rows."""
 import numpy as np
+import torch
 
 import workloads as W
 
@@ -33,3 +34,24 @@ def test_nan_poison():
     inp = W.custom(B=1, T=4, Tmax=16, start_pos=[3], junk="nan")
     ck = inp.cache_k.float().numpy()
     assert np.all(np.isnan(ck[0, 3:])) and not np.any(np.isnan(ck[0, :3]))
+
+
+def test_page_table_is_a_scattered_injection():
+    table, n_pages = W.page_table(3, 6, [2, 6, 0], spare=4, seed=9)
+    assert table.shape == (3, 6) and table.dtype == torch.int32 and n_pages == 12
+    used = table[table >= 0].tolist()
+    assert len(used) == 8 and len(set(used)) == 8 and all(0 <= x < n_pages for x in used)  # distinct, in range
+    assert (table[0, 2:] == -1).all() and (table[2] == -1).all()                         # entries past need
+    assert W.pages_needed([0, 1, 128, 129, 8192]).tolist() == [0, 1, 1, 2, 64]
+
+
+def test_to_pages_and_from_pages_round_trip():
+    B, Tmax = 2, 300  # Tmax not a multiple of the page size: the last page is partly filler
+    cache = torch.arange(B * Tmax * 8 * 128, dtype=torch.float32).remainder(997).to(torch.bfloat16)
+    cache = cache.view(B, Tmax, 8, 128)
+    table, n_pages = W.page_table(B, 3, [3, 3], spare=2, seed=10)
+    pool = W.to_pages(cache, table, n_pages, seed=11)
+    assert pool.shape == (n_pages, W.PAGE_TOKENS, 8, 128)
+    for b in range(B):
+        assert torch.equal(W.from_pages(pool, table, b, Tmax), cache[b])
+        assert torch.equal(pool[table[b, 1]], cache[b, 128:256])   # a page holds its 128 consecutive rows
