@@ -17,8 +17,14 @@ grok_status fail(grok_status s, const char* fmt, ...) {
   return s;
 }
 
+grok_status device_index(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(GROK_ERR_UNSUPPORTED, "device index %d out of range", *dev);
+  return GROK_OK;
+}
+
 grok_status device_sm_count(int* sm_count) {
-  constexpr int kMaxDevices = 64;
   static int cache[kMaxDevices] = {0};  // 0 = unknown, -1 = unsupported, else SM count
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

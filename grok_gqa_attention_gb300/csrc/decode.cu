@@ -323,11 +323,13 @@ static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src,
   const uint32_t box[4] = {64, 1, kDecKeysPerStage, 1};
   if ((st = encode_tmap_bf16_4d(&tk, k_src, dims, strides, box)) != GROK_OK) return st;
   if ((st = encode_tmap_bf16_4d(&tv, v_src, dims, strides, box)) != GROK_OK) return st;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};  // per device; idempotent: every thread would set the same value
+  int dev = 0;
+  if ((st = device_index(&dev)) != GROK_OK) return st;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set = true;
+    attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ns, kKVHeads, B);

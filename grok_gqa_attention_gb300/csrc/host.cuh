@@ -21,6 +21,11 @@ inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // The current device must be compute capability 10.3; returns its SM count.
 grok_status device_sm_count(int* sm_count);
 
+// Index of the current device, for one-time setup that must be repeated on
+// every device (function attributes live in each device's context).
+constexpr int kMaxDevices = 64;
+grok_status device_index(int* dev);
+
 // Launch-error check after a kernel launch.
 grok_status check_launch(const char* what);
 

@@ -595,11 +595,14 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
   prm.valid_len = valid_len;
   prm.status = dev_status;
 
-  static bool attr_set = false;  // idempotent: every thread would set the same value
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};  // per device; idempotent: every thread would set the same value
+  int dev = 0;
+  grok_status dst = device_index(&dev);
+  if (dst != GROK_OK) return dst;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const int grid = prm.n_items < sms ? prm.n_items : sms;
   prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);

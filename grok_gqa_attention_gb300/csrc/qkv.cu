@@ -471,11 +471,13 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   prm.n_tiles = prm.n_mtiles * prm.n_ntiles;
   const int grid = prm.n_tiles < sms ? prm.n_tiles : sms;
   auto kernel = fused ? qkv_kernel<true> : qkv_kernel<false>;
-  static bool attr_set[2] = {false, false};  // idempotent: every thread would set the same value
-  if (!attr_set[fused]) {
+  static bool attr_set[kMaxDevices][2] = {};  // per device and epilogue; idempotent
+  int dev = 0;
+  if ((st = device_index(&dev)) != GROK_OK) return st;
+  if (!attr_set[dev][fused]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem);
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set[fused] = true;
+    attr_set[dev][fused] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -563,12 +565,14 @@ static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w
   // An SM's shared-memory / L1 split is set for the blocks it runs: with the
   // default split for this small-smem kernel, the projection's CTAs could not
   // join its SMs before the table blocks finished.
-  static bool tab_attr_set = false;  // idempotent: every thread would set the same value
-  if (!tab_attr_set) {
+  static bool tab_attr_set[kMaxDevices] = {};  // per device; idempotent
+  int dev = 0;
+  if ((st0 = device_index(&dev)) != GROK_OK) return st0;
+  if (!tab_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(qkv_table_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          int(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    tab_attr_set = true;
+    tab_attr_set[dev] = true;
   }
   qkv_table_kernel<<<tab_grid, kQkvTabThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       start_pos, int(M), T, Tmax, const_cast<float*>(prm.cos_tab), const_cast<float*>(prm.sin_tab), dev_status);

@@ -179,14 +179,16 @@ static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const g
                            : rope_kv_append_kernel<1>;
   // Few tokens (a decode step): the SMs' shared-memory split is set for the
   // decode kernel that may join them, not for this kernel's 2 KB.
-  static bool carve_set = false;  // idempotent: every thread would set the same values
-  if (!carve_set) {
+  static bool carve_set[kMaxDevices] = {};  // per device; idempotent: every thread would set the same values
+  int dev = 0;
+  if ((st = device_index(&dev)) != GROK_OK) return st;
+  if (!carve_set[dev]) {
     for (auto kf : {rope_kv_append_kernel<8>, rope_kv_append_kernel<4>, rope_kv_append_kernel<2>}) {
       cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout,
                                            int(cudaSharedmemCarveoutMaxShared));
       if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     }
-    carve_set = true;
+    carve_set[dev] = true;
   }
   kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
