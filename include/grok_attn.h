@@ -286,6 +286,9 @@ grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, in
  *   grok_linear (so K % 64 == 0, N % 256 == 0). For prefill-sized M the
  *   product is tensor-bound and the one pass over the weight costs a few
  *   percent; the workspace may be reused across calls with the same weight.
+ *   For decode-sized M (M <= 32, K a multiple of 512, N of 64) the weight is
+ *   instead read once and dequantized on chip, the same per-element rounding,
+ *   and the workspace is not touched (it must still be passed).
  * All pointers device-resident and 16-byte aligned; w16, the workspace and y
  * 32-byte aligned. Asynchronous on stream.
  */
