@@ -7,6 +7,7 @@ import numpy as np
 import torch
 
 from oracle import bf16, projection as P, rope
+from tests.exact_util import nearest_bf16, nearest_f32
 
 
 ONE = np.uint16(0x3F80)  # bf16 1.0
@@ -14,20 +15,6 @@ ONE = np.uint16(0x3F80)  # bf16 1.0
 
 def _rand_bf16(rng, shape, scale=1.0):
     return bf16.from_f32((rng.standard_normal(shape) * scale).astype(np.float32))
-
-
-def _nearest_bf16_of_fraction(v: Fraction) -> float:
-    """Brute force: the bf16 value nearest the exact rational (ties to the even pattern)."""
-    f = float(v)
-    base = int(np.float32(f).view(np.uint32) >> 16)
-    cands = []
-    for d in (-2, -1, 0, 1, 2):
-        b = (base + d) & 0xFFFF
-        val = float(bf16.to_f64(np.array([b], dtype=np.uint16))[0])
-        if np.isfinite(val):
-            cands.append((abs(Fraction(val) - v), b % 2, val))
-    cands.sort()
-    return cands[0][2]
 
 
 def test_linear_equals_exact_rational_brute_force():
@@ -40,7 +27,7 @@ def test_linear_equals_exact_rational_brute_force():
         for t in range(3):
             for n in range(4):
                 exact = sum(Fraction(float(xf[a, t, i])) * Fraction(float(wf[i, n])) for i in range(5))
-                assert got[a, t, n] == _nearest_bf16_of_fraction(exact)
+                assert got[a, t, n] == nearest_bf16(exact)
 
 
 def test_identity_weights_return_x():
@@ -135,7 +122,7 @@ def test_dequant_int8_matches_exact_products_rounded_twice():
         for n in range(5):
             exact = float(w8[i, n]) * float(scales[n])          # exact in fp64
             r32 = float(np.float32(exact))
-            assert got[i, n] == _nearest_bf16_of_fraction(Fraction(r32))
+            assert got[i, n] == nearest_bf16(Fraction(r32))
 
 
 def test_dequant_int8_unit_and_power_of_two_scales_are_exact():
@@ -157,3 +144,34 @@ def test_linear_int8_is_linear_on_the_dequantized_weight():
     a, b = bf16.to_f64(P.linear_int8(x, w8, scales)), bf16.to_f64(P.linear_int8(x, w8, s2))
     assert np.array_equal(b[..., 7], 4.0 * a[..., 7])
     assert np.array_equal(np.delete(a, 7, axis=-1), np.delete(b, 7, axis=-1))
+
+
+def test_dequant_int8_two_roundings_at_decisive_elements():
+    """Where rounding w * s straight to bf16 would give another value than rounding it to
+    fp32 first (ch. 4 §4.1: ``astype(scales.dtype) * scales``, then the cast to bf16), the
+    oracle takes the two roundings. Such elements are built directly: for a bf16 midpoint
+    tau and an int8 w that is not a power of two, an fp32 scale next to tau / w makes the
+    exact product lie just off tau while its fp32 rounding is tau itself."""
+    rng = np.random.default_rng(30)
+    ties = ((rng.integers(0x3880, 0x3F80, size=256).astype(np.uint32) << 16) | 0x8000).view(np.float32)
+    odd = [v for v in range(-127, 128) if v and abs(v) & (abs(v) - 1)]
+    ws, ss = [], []
+    for tau, w in zip(ties, rng.choice(odd, size=len(ties))):
+        s0 = np.float32(float(tau) / int(w))
+        for k in range(-3, 4):
+            sc = s0
+            for _ in range(abs(k)):
+                sc = np.nextafter(sc, np.float32(np.inf if k > 0 else -np.inf))
+            exact = Fraction(int(w)) * Fraction(float(sc))
+            if nearest_f32(exact) == Fraction(float(tau)) and nearest_bf16(Fraction(float(tau))) != nearest_bf16(exact):
+                ws.append(int(w))
+                ss.append(sc)
+                break
+        if len(ws) == 24:
+            break
+    assert len(ws) == 24
+    got = bf16.to_f64(P.dequant_int8(np.array(ws, dtype=np.int8)[None, :], np.array(ss, dtype=np.float32)))[0]
+    for k, (w, sc) in enumerate(zip(ws, ss)):
+        exact = Fraction(w) * Fraction(float(sc))
+        assert got[k] == nearest_bf16(nearest_f32(exact))
+        assert got[k] != nearest_bf16(exact)                     # the case is decisive

@@ -1,10 +1,12 @@
 """Pins of the oracle's RoPE and cache append (closed forms, invariants, the pages' examples)."""
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
 
 from oracle import bf16, rope
+from tests.exact_util import nearest_bf16, nearest_f32
 
 
 def _rand_bf16(rng, shape, scale=3.0):
@@ -137,3 +139,42 @@ def test_rope_kv_append_rotates_k_not_v():
     assert np.array_equal(nk[0, 10:14], rope.rotary_embedding(k, start)[0])
     assert np.array_equal(q_rot, rope.rotary_embedding(q, start))
     assert not np.array_equal(nk[0, 10:14], k[0])
+
+
+def _rotated_brute_force(x_f, t: int, i: int, freqs) -> float:
+    """One output feature by exact rationals: the pages' fp32 chain, each step rounded on its own."""
+    dim = len(x_f)
+    ph = nearest_f32(Fraction(t) * Fraction(float(freqs[i % (dim // 2)])))    # fp32 t * fp32 inv_freq
+    c = nearest_f32(Fraction(math.cos(float(ph))))
+    s = nearest_f32(Fraction(math.sin(float(ph))))
+    partner = -x_f[i + dim // 2] if i < dim // 2 else x_f[i - dim // 2]      # rotate_half
+    a = nearest_f32(Fraction(float(x_f[i])) * c)
+    b = nearest_f32(Fraction(float(partner)) * s)
+    return nearest_bf16(nearest_f32(a + b))
+
+
+def test_rotation_follows_the_fp32_rounding_chain_exactly():
+    """ch. 4 §4.3.1 in the pages' dtypes: fp32 positions and inv_freq, their fp32 product as
+    the phase, fp32 cos and sin, bf16 x promoted to fp32, x*cos and rotate_half(x)*sin and
+    their sum each rounded to fp32, then the cast to bf16. Checked by exact-rational brute
+    force near the largest position, on random elements and on the elements where rounding
+    the products and the sum only once would change the bf16 result."""
+    rng = np.random.default_rng(17)
+    T, H, off = 2048, 8, rope.MAX_POSITION - 2048
+    x = _rand_bf16(rng, (1, T, H, 128))
+    y = bf16.to_f64(rope.rotary_embedding(x, np.array([off])))
+    freqs = rope.inv_freq(128)          # pinned on its own by the closed form above
+    xf = bf16.to_f32(x)[0]
+    # selection only: elements where one rounding of x*c + rh*s differs from three
+    t = np.arange(T, dtype=np.float32) + np.float32(off)
+    ph = (t[:, None] * freqs[None, :]).astype(np.float32)
+    ph = np.concatenate((ph, ph), axis=-1)[:, None, :].astype(np.float64)
+    c, s = np.cos(ph).astype(np.float32), np.sin(ph).astype(np.float32)
+    rh = np.concatenate((-xf[..., 64:], xf[..., :64]), axis=-1)
+    once = bf16.from_f64(xf.astype(np.float64) * c + rh.astype(np.float64) * s)
+    thrice = bf16.from_f32((xf * c).astype(np.float32) + (rh * s).astype(np.float32))
+    decisive = [tuple(e) for e in np.argwhere(once != thrice)[:16]]
+    assert len(decisive) >= 8
+    picks = decisive + [tuple(int(v) for v in rng.integers((T, H, 128))) for _ in range(96)]
+    for ti, h, i in picks:
+        assert y[0, ti, h, i] == _rotated_brute_force(xf[ti, h], off + ti, i, freqs), (ti, h, i)
