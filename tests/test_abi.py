@@ -99,3 +99,33 @@ def test_misaligned_outputs_rejected_before_any_device_call(lib):
     assert lib.grok_linear(a32, a32, 256, 64, 256, a16, None, None) == 1
     assert b"32-byte" in lib.grok_last_error()
     assert lib.grok_dequant_int8(a32, a32, 64, 256, a16, None) == 1
+
+
+def test_product_path_has_no_cpu_route():
+    """The binding computes nothing itself: CPU tensors are refused, a missing library
+    raises, and no file of the package or its CUDA sources refers to the oracle."""
+    import torch
+
+    import grok_gqa_attention_gb300 as G
+    q = torch.zeros((1, 4, 48, 128), dtype=torch.bfloat16)
+    kv = torch.zeros((1, 4, 8, 128), dtype=torch.bfloat16)
+    cache = torch.zeros((1, 8, 8, 128), dtype=torch.bfloat16)
+    start = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        G.rope_kv_append(q, kv, kv, start, torch.empty_like(q), cache, cache.clone())
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        G.prefill(q, cache, cache, start, None, torch.empty_like(q))
+    pkg = os.path.join(ROOT, "grok_gqa_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for name in files:
+            if name.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, name)).read()
+                assert not re.search(r"\boracle\b", text), f"{name} refers to the oracle"
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    import grok_gqa_attention_gb300 as G
+    monkeypatch.setattr(G, "_lib", None)
+    monkeypatch.setattr(G, "LIB_PATH", str(tmp_path / "libgrok_attn.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        G.load()
