@@ -245,7 +245,7 @@ class OraclePool:
         self.pool.join()
 
 
-def cpu_baseline(n_tokens: int = 64) -> dict:
+def cpu_baseline(n_tokens: int = 512) -> dict:
     pool = OraclePool(PREFILL_WORKLOAD)
     try:
         r, wall, used = pool.rate(n_tokens, seed=0)
