@@ -208,3 +208,17 @@ def test_chain_mode_sits_near_exact():
     d = np.abs(ex - ch)
     assert d.max() <= 0.0625 + 1e-12
     assert 1e-4 < d.mean() < 5e-3
+
+
+def test_full_attention_covers_rows_across_its_row_blocks():
+    """attention() evaluates rows in blocks of ROW_BLOCK; at T > ROW_BLOCK every row,
+    including those either side of a block edge, equals the one-row evaluation."""
+    rng = np.random.default_rng(17)
+    T = A.ROW_BLOCK + 44
+    q, ck, cv, start = _tiny_case(rng, B=1, T=T, Tmax=T)
+    full = A.attention(q, ck, cv, start, None)
+    edge = [0, A.ROW_BLOCK - 2, A.ROW_BLOCK - 1, A.ROW_BLOCK, T - 1]
+    rows = [(0, i, h) for i in edge for h in (0, 23, 47)]
+    bits, _ = A.attention_rows(q, ck, cv, start, np.array([T]), T, rows)
+    for n, (b, i, h) in enumerate(rows):
+        assert np.array_equal(bits[n], full[b, i, h]), (i, h)

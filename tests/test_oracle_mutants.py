@@ -82,6 +82,7 @@ MUTANTS = [
      [("np.arange(T, dtype=np.float32)", "np.arange(1, T + 1, dtype=np.float32)")]),
     ("cos_and_sin_swapped", R, "rotary_embedding",
      [("a = (x * c)", "a = (x * s)"), ("b = (rotate_half(x) * s)", "b = (rotate_half(x) * c)")]),
+    ("cos_sin_left_in_fp64", R, "cos_sin", [("return c.astype(np.float32), s.astype(np.float32)", "return c, s")]),
     ("phase_in_fp64", R, "phase",
      [("(t[:, :, None] * freqs[None, None, :]).astype(np.float32)",
        "t[:, :, None].astype(np.float64) * freqs[None, None, :].astype(np.float64)")]),
@@ -120,6 +121,10 @@ MUTANTS = [
     ("valid_len_ignored", A, "attention",
      [("valid = np.full(B, T) if valid is None else np.asarray(valid)", "valid = np.full(B, T)")]),
     ("decode_at_kv_len", A, "decode", [("kv_len - 1, None, mode", "kv_len, None, mode")]),
+    ("row_block_skips_its_last_row", A, "attention",
+     [("np.arange(i0, min(T, i0 + ROW_BLOCK))", "np.arange(i0, min(T, i0 + ROW_BLOCK - 1))")]),
+    ("rows_ignore_start", A, "attention_rows", [("s, nv = int(start[b]), int(valid[b])", "s, nv = 0, int(valid[b])")]),
+    ("group_is_kv_head_count", A, "_kv_heads", [("return n_q, n_q // n_kv", "return n_q, n_kv")]),
     # projections
     ("k_and_v_columns_swapped", P, "qkv_projection",
      [("k = y[..., nq:nq + nk].reshape(B, T, N_KV_HEADS, HEAD_DIM)\n    v = y[..., nq + nk:]",
