@@ -28,11 +28,19 @@ DEV_BAD_PAGE = 0x10
 
 PAGE_TOKENS = 128
 
+# grok_status values (include/grok_attn.h)
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 3
+ERR_DEVICE_FAULT = 4
+
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgrok_attn.so")
 
 EXPORTS = (
     "grok_abi_version",
     "grok_last_error",
+    "grok_cuda_error_status",
     "grok_rope_kv_append",
     "grok_rope_cos_sin",
     "grok_attn_prefill",
@@ -83,6 +91,8 @@ def load() -> ctypes.CDLL:
     lib.grok_abi_version.argtypes = []
     lib.grok_last_error.restype = ctypes.c_char_p
     lib.grok_last_error.argtypes = []
+    lib.grok_cuda_error_status.restype = I
+    lib.grok_cuda_error_status.argtypes = [I]
     lib.grok_rope_kv_append.restype = I
     lib.grok_rope_kv_append.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P]
     lib.grok_rope_cos_sin.restype = I

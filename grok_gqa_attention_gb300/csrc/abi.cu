@@ -17,9 +17,33 @@ grok_status fail(grok_status s, const char* fmt, ...) {
   return s;
 }
 
+grok_status cuda_status(cudaError_t e) {
+  switch (e) {
+    case cudaSuccess:
+      return GROK_OK;
+    case cudaErrorECCUncorrectable:
+    case cudaErrorNvlinkUncorrectable:
+    case cudaErrorContained:
+    case cudaErrorIllegalAddress:
+    case cudaErrorLaunchTimeout:
+    case cudaErrorAssert:
+    case cudaErrorHardwareStackError:
+    case cudaErrorIllegalInstruction:
+    case cudaErrorMisalignedAddress:
+    case cudaErrorInvalidAddressSpace:
+    case cudaErrorInvalidPc:
+    case cudaErrorLaunchFailure:
+    case cudaErrorTensorMemoryLeak:
+    case cudaErrorExternalDevice:
+      return GROK_ERR_DEVICE_FAULT;
+    default:
+      return GROK_ERR_CUDA;
+  }
+}
+
 grok_status device_index(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "cudaGetDevice: %s", cudaGetErrorString(e));
   if (*dev < 0 || *dev >= kMaxDevices) return fail(GROK_ERR_UNSUPPORTED, "device index %d out of range", *dev);
   return GROK_OK;
 }
@@ -28,7 +52,7 @@ grok_status device_sm_count(int* sm_count) {
   static int cache[kMaxDevices] = {0};  // 0 = unknown, -1 = unsupported, else SM count
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) {
     *sm_count = cache[dev];
     return GROK_OK;
@@ -37,7 +61,7 @@ grok_status device_sm_count(int* sm_count) {
   if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return fail(GROK_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    return fail(cuda_status(e), "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
   if (major != 10 || minor != 3)
     return fail(GROK_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
                 major, minor);
@@ -48,7 +72,7 @@ grok_status device_sm_count(int* sm_count) {
 
 grok_status check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "%s launch: %s", what, cudaGetErrorString(e));
   return GROK_OK;
 }
 
@@ -90,3 +114,7 @@ grok_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64
 extern "C" int grok_abi_version(void) { return GROK_ATTN_ABI_VERSION; }
 
 extern "C" const char* grok_last_error(void) { return grok::g_error; }
+
+extern "C" grok_status grok_cuda_error_status(int cuda_error) {
+  return grok::cuda_status(static_cast<cudaError_t>(cuda_error));
+}

@@ -328,7 +328,7 @@ static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src,
   if ((st = device_index(&dev)) != GROK_OK) return st;
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -343,7 +343,7 @@ static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src,
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, tk, tv, reinterpret_cast<const uint32_t*>(q_rot), kv_len,
                                      kv_add, Tmax, ns, dec_ws(workspace, B, ns), pm, dev_status);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "decode launch: %s", cudaGetErrorString(e));
   return check_launch("decode");
 }
 
@@ -362,7 +362,7 @@ static grok_status combine_launch(const void* workspace, const int32_t* kv_len, 
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, dec_ws(const_cast<void*>(workspace), B, ns), kv_len,
                                      kv_add, Tmax, ns, reinterpret_cast<uint2*>(out), dev_status);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "combine launch: %s", cudaGetErrorString(e));
   return check_launch("combine");
 }
 
@@ -419,9 +419,11 @@ extern "C" grok_status grok_attn_combine(const void* workspace, size_t workspace
 // owns every byte of device memory and gives its plugins no allocator, or a
 // serving loop whose memory plan is fixed up front and where cudaMalloc, which
 // may synchronise the device and take milliseconds, is not allowed between
-// steps. For them the split-K partial sums live in this file-scope array. It
-// is allocated when the library is loaded, on every GPU that loads it, and
-// held until the process exits.
+// steps. For them the split-K partial sums live in this file-scope array.
+// CUDA loads device code lazily by default, so a device reserves the array
+// when the library's code is first used on it (possibly by the first call of
+// grok_attn_decode_step_static) and holds it until the process exits; callers
+// make one warm-up call per device before fixing their memory plan.
 static __device__ __align__(256) unsigned char g_static_ws[GROK_STATIC_WORKSPACE_BYTES];
 
 namespace {
@@ -434,14 +436,14 @@ void* g_static_ptr[64] = {nullptr};
 grok_status static_ws_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return fail(GROK_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_static_mu);
   if (!g_static_ptr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_ws);
     if (e != cudaSuccess || !p)
-      return fail(GROK_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
+      return fail(cuda_status(e), "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
     g_static_ptr[dev] = p;
   }
   *out = g_static_ptr[dev];
@@ -468,7 +470,9 @@ extern "C" grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, cons
   grok_status st = static_ws_address(&ws);
   if (st != GROK_OK) return st;
   // Every partial sum the combine reads is written by the decode launch just
-  // before it, so the scratch needs no clearing between calls.
+  // before it, so the scratch needs no clearing between calls. (A decode CTA
+  // whose bounded wait gives up skips its writes and reports GROK_DEV_TIMEOUT;
+  // the output is then undefined, as documented.)
   if ((st = grok_attn_decode(q_rot, cache_k, cache_v, kv_len, B, Tmax, ws, need, dev_status, stream)) != GROK_OK)
     return st;
   return grok_attn_combine(ws, need, kv_len, B, Tmax, out, dev_status, stream);

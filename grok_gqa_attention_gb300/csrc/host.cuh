@@ -14,6 +14,10 @@ namespace grok {
 // Record a message for grok_last_error() and return `s`.
 grok_status fail(grok_status s, const char* fmt, ...);
 
+// Status for a failed CUDA runtime call: GROK_ERR_DEVICE_FAULT for the sticky
+// errors that leave the context unusable, GROK_ERR_CUDA otherwise.
+grok_status cuda_status(cudaError_t e);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // Outputs written with 32-byte stores (st.global.v8.b32) need 32-byte alignment.
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }

@@ -69,7 +69,7 @@ void release(grok_prefill_pipe* p) {
 }
 
 grok_status cuda_fail(const char* what, cudaError_t e) {
-  return fail(GROK_ERR_CUDA, "grok_prefill_pipe: %s: %s", what, cudaGetErrorString(e));
+  return fail(cuda_status(e), "grok_prefill_pipe: %s: %s", what, cudaGetErrorString(e));
 }
 
 }  // namespace

@@ -601,7 +601,7 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
   if (dst != GROK_OK) return dst;
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev] = true;
   }
   const int grid = prm.n_items < sms ? prm.n_items : sms;

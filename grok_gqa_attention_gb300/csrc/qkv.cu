@@ -594,7 +594,7 @@ static grok_status linear_int8_small(const grok_bf16* x, const int8_t* w8, const
   auto kernel = mt == 1 ? linear_int8_small_kernel<1> : linear_int8_small_kernel<2>;
   if (!attr_set[dev][mt - 1]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev][mt - 1] = true;
   }
   kernel<<<unsigned(N / kSmCols), kSmThreads, smem, static_cast<cudaStream_t>(stream)>>>(
@@ -635,7 +635,7 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   if ((st = device_index(&dev)) != GROK_OK) return st;
   if (!attr_set[dev][fused]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem);
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev][fused] = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -649,7 +649,7 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, prm);
-  if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "qkv launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(cuda_status(e), "qkv launch: %s", cudaGetErrorString(e));
   return check_launch("qkv");
 }
 
@@ -730,7 +730,7 @@ static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w
   if (!tab_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(qkv_table_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          int(cudaSharedmemCarveoutMaxShared));
-    if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     tab_attr_set[dev] = true;
   }
   qkv_table_kernel<<<tab_grid, kQkvTabThreads, 0, static_cast<cudaStream_t>(stream)>>>(

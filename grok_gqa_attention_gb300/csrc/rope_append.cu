@@ -186,7 +186,7 @@ static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const g
     for (auto kf : {rope_kv_append_kernel<8>, rope_kv_append_kernel<4>, rope_kv_append_kernel<2>}) {
       cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout,
                                            int(cudaSharedmemCarveoutMaxShared));
-      if (e != cudaSuccess) return fail(GROK_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     }
     carve_set[dev] = true;
   }

@@ -33,16 +33,23 @@
  *     innermost dimension contiguous and no padding:
  *       q, q_rot, out  [B, T, 48, 128]      k, v  [B, T, 8, 128]
  *       cache_k/v      [B, Tmax, 8, 128]
- *   - every pointer argument is a DEVICE pointer owned by the caller; the
- *     library never allocates, frees or retains caller memory, and every
- *     pointer to a bf16 tensor must be 16-byte aligned (32-byte for the outputs
- *     of the projection, Linear and dequant calls below, which are written with
- *     32-byte stores).
+ *   - every pointer argument is a DEVICE pointer owned by the caller (except
+ *     the host buffers of the prefill pipeline); the library never frees or
+ *     retains caller memory, and every pointer to a bf16 tensor must be 16-byte
+ *     aligned (32-byte for the outputs of the projection, Linear and dequant
+ *     calls below, which are written with 32-byte stores).
+ *   - no call allocates device memory except grok_prefill_pipe_create, which
+ *     allocates the pipeline's buffers once (freed by grok_prefill_pipe_destroy).
+ *     Scratch space is a caller-owned workspace whose size a *_workspace call
+ *     gives, or, for grok_attn_decode_step_static, a static array of the library.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every call
  *     is asynchronous on it and returns after enqueueing its kernels.
  *   - errors found on the host (null or misaligned pointers, bad sizes) return
- *     GROK_ERR_INVALID_ARG before anything is launched; a failed launch returns
- *     GROK_ERR_CUDA. grok_last_error() then describes it (thread-local).
+ *     GROK_ERR_INVALID_ARG before anything is launched; a failed CUDA call or
+ *     launch returns GROK_ERR_CUDA, or GROK_ERR_DEVICE_FAULT when the error is
+ *     a sticky one that has left the CUDA context unusable (an earlier kernel's
+ *     illegal address, say: every later call then reports it).
+ *     grok_last_error() then describes it (thread-local).
  *   - errors that depend on device data (positions, lengths) or a bounded wait
  *     that gave up are OR-ed into *dev_status (a device int32 the caller zeroes;
  *     NULL disables reporting) as GROK_DEV_* bits. The kernels never trap or
@@ -75,8 +82,12 @@ typedef uint16_t grok_bf16;
 typedef enum {
   GROK_OK = 0,
   GROK_ERR_INVALID_ARG = 1,
-  GROK_ERR_UNSUPPORTED = 2, /* no sm_103 device, or a size this build does not cover */
-  GROK_ERR_CUDA = 3         /* a CUDA runtime or driver call failed */
+  GROK_ERR_UNSUPPORTED = 2,  /* no sm_103 device, or a size this build does not cover */
+  GROK_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed; the context is still usable */
+  GROK_ERR_DEVICE_FAULT = 4  /* a sticky device error (illegal address or instruction, misaligned
+                                address, launch failure, uncorrectable ECC or NVLink error, ...):
+                                the CUDA context is dead and every later call fails the same way;
+                                the process must be restarted to use the GPU again */
 } grok_status;
 
 /* bits OR-ed into *dev_status by the kernels */
@@ -94,6 +105,14 @@ int grok_abi_version(void);
 
 /* Message describing the last non-OK status returned on this thread. */
 const char* grok_last_error(void);
+
+/*
+ * The status this library returns when a CUDA runtime call fails with
+ * `cuda_error` (a cudaError_t value): GROK_OK for cudaSuccess,
+ * GROK_ERR_DEVICE_FAULT for the errors that leave the context unusable,
+ * GROK_ERR_CUDA for the rest. Host only; touches no device.
+ */
+grok_status grok_cuda_error_status(int cuda_error);
 
 /*
  * RoPE on Q and K, then the KV-cache append (ch. 4 §4.3.1, §4.4).
@@ -168,7 +187,12 @@ grok_status grok_attn_decode(const grok_bf16* q_rot, const grok_bf16* cache_k, c
 /*
  * Decode step, combine part: out[b, h] = (sum over splits of o) / (sum over
  * splits of l), rounded to bf16. Reads the workspace written by
- * grok_attn_decode with the same B, Tmax and kv_len.
+ * grok_attn_decode with the same B, Tmax and kv_len. workspace_bytes is the
+ * size of that workspace, checked against grok_attn_decode_workspace(B, Tmax)
+ * before anything is launched (the pages' interface has no workspace; the
+ * size travels with the pointer so that a short buffer is an argument error,
+ * not an out-of-bounds read). If grok_attn_decode set a bit in *dev_status
+ * (a bounded wait that gave up skips a split's writes), out is undefined.
  *   out [B,48,128] bf16.
  */
 grok_status grok_attn_combine(const void* workspace, size_t workspace_bytes, const int32_t* kv_len, int B,
@@ -198,16 +222,22 @@ grok_status grok_selftest_bounded_wait(int32_t* dev_status, int32_t* flags, long
  * synchronise the device) between steps.
  *
  * The split-K partial sums go to a static device array of
- * GROK_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
- * the process exits; shapes whose workspace (grok_attn_decode_workspace) is
- * larger are rejected with GROK_ERR_INVALID_ARG. The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current, so make the first call on each device before any stream capture.
+ * GROK_STATIC_WORKSPACE_BYTES; shapes whose workspace (grok_attn_decode_workspace)
+ * is larger are rejected with GROK_ERR_INVALID_ARG. CUDA loads the library's
+ * device code lazily by default (CUDA_MODULE_LOADING=LAZY), so the array is
+ * reserved on a device when the library's code is first used there, possibly
+ * by the first call of this function, and held until the process exits. The
+ * first call on a device also looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current. So make one warm-up call on
+ * each device at initialisation, before the memory plan is fixed and before
+ * any stream capture; later calls allocate nothing.
  * All calls share the one array: calls that overlap on the GPU (different
  * streams, or different host threads on the same device) race and give wrong
  * results; calls ordered on one stream are safe. Nothing needs clearing: each
- * call writes every partial sum it reads. Arguments and results are those of
- * grok_attn_decode + grok_attn_combine:
+ * call that completes writes every partial sum it reads. If *dev_status comes
+ * back nonzero (a bad kv_len, or a bounded wait that gave up), out is undefined
+ * for this call and may hold values computed from an earlier call's partial
+ * sums. Arguments and results are those of grok_attn_decode + grok_attn_combine:
  *   q_rot [B,48,128]; cache_k, cache_v [B,Tmax,8,128]; kv_len [B] int32; out [B,48,128].
  */
 grok_status grok_attn_decode_step_static(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,

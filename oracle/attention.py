@@ -172,6 +172,29 @@ def attention_rows(q_rot_bits, cache_k_bits, cache_v_bits, start, valid, T, rows
     return bf16.from_f64(out), out
 
 
+def attention_block(q_rot_bits, cache_k_bits, cache_v_bits, start, valid, T, b, i0, i1):
+    """The same definition for query rows [i0, i1) of sequence b, every head.
+
+    Returns bf16 bits [i1 - i0, Hq, d]. Used to check whole query tiles at sizes
+    where the full output is too slow on the CPU.
+    """
+    n_q, group = _kv_heads(q_rot_bits, cache_k_bits)
+    B = q_rot_bits.shape[0]
+    valid = np.full(B, T) if valid is None else np.asarray(valid)
+    s, n = int(start[b]), int(valid[b])
+    L = s + T
+    rows = np.arange(i0, i1)
+    mask = visible(s, n, T, rows, L)
+    out = np.zeros((len(rows), n_q, q_rot_bits.shape[-1]), dtype=np.float64)
+    for h in range(n_q):
+        g = h // group
+        K = bf16.to_f64(cache_k_bits[b, :L, g, :])
+        V = bf16.to_f64(cache_v_bits[b, :L, g, :])
+        q = bf16.to_f64(q_rot_bits[b, rows, h, :])
+        out[:, h, :] = _attend_exact(q, K, V, mask)
+    return bf16.from_f64(out)
+
+
 def decode(q_rot_bits, cache_k_bits, cache_v_bits, kv_len, mode="exact", return_f64=False):
     """One decode step: q_rot [B, Hq, d] at position kv_len[b]-1 over cache rows < kv_len[b].
 

@@ -129,3 +129,20 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(G, "LIB_PATH", str(tmp_path / "libgrok_attn.so"))
     with pytest.raises(RuntimeError, match="missing"):
         G.load()
+
+
+def test_sticky_cuda_errors_map_to_device_fault(lib):
+    """A CUDA error that kills the context is reported as GROK_ERR_DEVICE_FAULT, every
+    other failure as GROK_ERR_CUDA (cudaError_t values of the CUDA 13 runtime)."""
+    import grok_gqa_attention_gb300 as G
+    assert lib.grok_cuda_error_status(0) == G.OK
+    sticky = {"illegal address": 700, "launch timeout": 702, "device assert": 710, "hardware stack": 714,
+              "illegal instruction": 715, "misaligned address": 716, "invalid address space": 717,
+              "invalid pc": 718, "launch failure": 719, "tensor memory leak": 721,
+              "uncorrectable ECC": 214, "uncorrectable NVLink": 220, "contained": 226, "external device": 911}
+    for what, code in sticky.items():
+        assert lib.grok_cuda_error_status(code) == G.ERR_DEVICE_FAULT, what
+    recoverable = {"invalid value": 1, "out of memory": 2, "invalid device function": 98,
+                   "no device": 100, "not ready": 600, "launch out of resources": 701, "unknown": 999}
+    for what, code in recoverable.items():
+        assert lib.grok_cuda_error_status(code) == G.ERR_CUDA, what

@@ -50,17 +50,36 @@ def _sample_rows(B, T, n, seed):
     return sorted(rows)
 
 
+def _whole_tiles(name, inp):
+    """(b, first row) of the 128-row query tiles checked in full, every head:
+    the first, a middle and the last tile of the long prefill; for the ragged
+    batch the tile holding each sequence's last valid row (where its key padding
+    starts); for the chunk on a warm cache both tiles of the first and last
+    sequence."""
+    w = inp.workload
+    if name == "prefill_b1_t8192":
+        return [(0, 0), (0, (w.T // 256) * 128), (0, w.T - 128)]
+    if name == "ragged_prefill_b8_t2048":
+        return [(b, ((int(n) - 1) // 128) * 128) for b, n in enumerate(inp.valid_len.numpy())]
+    return [(b, i0) for b in (0, w.B - 1) for i0 in range(0, w.T, 128)]
+
+
 @pytest.mark.parametrize("name", ["prefill_b1_t8192", "ragged_prefill_b8_t2048", "chunked_prefill_b4_t256_at6144"])
-def test_prefill_full_size_sampled_rows(name):
+def test_prefill_full_size_whole_tiles_and_sampled_rows(name):
     inp = cached_inputs(name)
     oq, ok_, ov, out, status = run_prefill(inp)
     assert status == 0
     rq, rk, rv = oracle_append(inp)
     assert np.array_equal(oq, rq) and np.array_equal(ok_, rk) and np.array_equal(ov, rv)
     w = inp.workload
-    rows = _sample_rows(w.B, w.T, 160, seed=1)
     valid = None if inp.valid_len is None else inp.valid_len.numpy()
-    ref, _ = A.attention_rows(rq, rk, rv, inp.start_pos.numpy(), valid, w.T, rows)
+    start = inp.start_pos.numpy()
+    for b, i0 in _whole_tiles(name, inp):
+        i1 = min(i0 + 128, w.T)
+        ref = A.attention_block(rq, rk, rv, start, valid, w.T, b, i0, i1)
+        assert_close(out[b, i0:i1], ref, f"{name} tile b={b} rows {i0}..{i1 - 1}")
+    rows = _sample_rows(w.B, w.T, 160, seed=1)
+    ref, _ = A.attention_rows(rq, rk, rv, start, valid, w.T, rows)
     got = np.stack([out[b, i, h] for (b, i, h) in rows])
     assert_close(got, ref, name)
     vals = W.from_bits(out).float()

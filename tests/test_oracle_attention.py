@@ -2,6 +2,7 @@
 KV heads, a library routine in the uncapped special case, closed forms of the
 soft cap and softmax, brute force on tiny inputs, decode = prefill row."""
 import math
+import struct
 
 import numpy as np
 import torch
@@ -210,6 +211,95 @@ def test_chain_mode_sits_near_exact():
     assert 1e-4 < d.mean() < 5e-3
 
 
+def test_chain_mode_closed_forms():
+    """The pages' dtype chain (ch. 4 §4.5.3: fp32 logits and softmax, weights cast
+    to bf16 before the weighted sum) on inputs whose result is known in closed form.
+
+    (a) Three keys with equal logits: each weight is RN32(1/3), which bf16 rounds
+    to 0.333984375, so with every value row equal to c the chain returns
+    3 * 0.333984375 * c (the exact method returns c).
+    (b) Two keys whose raw dot products are 256 and 257: fp32 keeps them apart,
+    bf16 would not (257 is a bf16 tie that rounds to 256). The weight of the
+    second key is 1 / (1 + exp(c0 - c1)) = 0.5131 with c = 30 tanh(s / sqrt(128) / 30),
+    which the chain returns to within one bf16 step (2^-8 on [0.5, 1)); bf16 logits
+    would give exactly 0.5.
+    """
+    d = 16
+    q = np.zeros((1, 3, 2, d), np.float32)
+    k = np.zeros((1, 3, 1, d), np.float32)
+    v = np.zeros((1, 3, 1, d), np.float32)
+    q[0, :, :, 0] = 1.0
+    k[0, :, 0, 0] = 2.0
+    v[0, :, 0, :] = 1.5
+    qb, kb, vb = (bf16.from_f32(x) for x in (q, k, v))
+    _, o = A.attention(qb, kb, vb, np.array([0]), None, mode="chain", return_f64=True)
+    assert np.all(o[0, 2] == 3 * 0.333984375 * 1.5)
+    _, o = A.attention(qb, kb, vb, np.array([0]), None, mode="exact", return_f64=True)
+    assert np.all(o[0, 2] == 1.5)
+
+    q = np.zeros((1, 2, 2, d), np.float32)
+    k = np.zeros((1, 2, 1, d), np.float32)
+    v = np.zeros((1, 2, 1, d), np.float32)
+    q[0, :, :, 0], q[0, :, :, 1] = 16.0, 1.0
+    k[0, 0, 0, 0], k[0, 1, 0, 0], k[0, 1, 0, 1] = 16.0, 16.0, 1.0
+    v[0, 1, 0, 0] = 1.0   # feature 0 returns the weight of key 1
+    v[0, 0, 0, 1] = 1.0   # feature 1 returns the weight of key 0
+    qb, kb, vb = (bf16.from_f32(x) for x in (q, k, v))
+    _, o = A.attention(qb, kb, vb, np.array([0]), None, mode="chain", return_f64=True)
+    c = 30 * np.tanh(np.array([256.0, 257.0]) / math.sqrt(128) / 30)
+    w1 = 1 / (1 + math.exp(c[0] - c[1]))
+    assert abs(o[0, 1, 0, 0] - w1) <= 2 ** -8 and abs(o[0, 1, 0, 1] - (1 - w1)) <= 2 ** -9
+    assert abs(o[0, 1, 0, 0] - 0.5) > 2 ** -8
+
+
+def _rn32(x: float) -> float:
+    """Round a Python float to the nearest binary32 (ties to even) through struct."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def _rn_bf16(x: float) -> float:
+    """Round a binary32 value to bfloat16 (nearest, ties to even) from its bits."""
+    u = struct.unpack("<I", struct.pack("<f", x))[0]
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return struct.unpack("<f", struct.pack("<I", (u & 0xFFFF) << 16))[0]
+
+
+def test_chain_mode_scalar_brute_force():
+    """Scalar evaluation of the pages' chain, each step rounded to fp32 on its own
+    (ch. 4 §4.5.2-§4.5.4): logits = fp32(q . k); fp32 multiply by fp32(1/sqrt(128));
+    fp32 division by 30, fp32 tanh, fp32 multiply by 30; masked logits -1e30;
+    fp32 max, fp32 exp of the fp32 difference, fp32 row sum left to right, fp32
+    division; weights to bf16; weighted sum of V. No numpy arithmetic is used for
+    the chain itself: fp32 rounding goes through struct, tanh and exp are the fp64
+    library functions rounded to fp32."""
+    rng = np.random.default_rng(18)
+    T, d, start, valid = 6, 8, 0, 5
+    q = _rand_bf16(rng, (1, T, 2, d), 2.0)
+    ck = _rand_bf16(rng, (1, T, 1, d), 2.0)
+    cv = _rand_bf16(rng, (1, T, 1, d), 1.0)
+    _, got = A.attention(q, ck, cv, np.array([start]), np.array([valid]), mode="chain", return_f64=True)
+    qf, kf, vf = (bf16.to_f64(x) for x in (q, ck, cv))
+    mult = _rn32(0.08838834764831845)
+    for i in range(T):
+        for h in range(2):
+            logits = []
+            for j in range(start + T):
+                s = _rn32(sum(qf[0, i, h, t] * kf[0, j, 0, t] for t in range(d)))
+                s = _rn32(s * mult)
+                s = _rn32(30.0 * _rn32(math.tanh(_rn32(s / 30.0))))
+                visible = j <= start + i and j < start + valid
+                logits.append(s if visible else _rn32(-1e30))
+            m = max(logits)
+            e = [_rn32(math.exp(_rn32(x - m))) for x in logits]
+            z = 0.0
+            for x in e:
+                z = _rn32(z + x)
+            w = [_rn_bf16(_rn32(x / z)) for x in e]
+            for t in range(d):
+                o = sum(w[j] * vf[0, j, 0, t] for j in range(start + T))
+                assert abs(got[0, i, h, t] - o) < 1e-12, (i, h, t)
+
+
 def test_full_attention_covers_rows_across_its_row_blocks():
     """attention() evaluates rows in blocks of ROW_BLOCK; at T > ROW_BLOCK every row,
     including those either side of a block edge, equals the one-row evaluation."""
@@ -222,3 +312,18 @@ def test_full_attention_covers_rows_across_its_row_blocks():
     bits, _ = A.attention_rows(q, ck, cv, start, np.array([T]), T, rows)
     for n, (b, i, h) in enumerate(rows):
         assert np.array_equal(bits[n], full[b, i, h]), (i, h)
+
+
+def test_block_api_matches_full():
+    """attention_block (whole query tiles, every head) equals the full evaluation,
+    on a block that straddles the full evaluation's row blocks, for a chunk on a
+    warm cache with key padding."""
+    rng = np.random.default_rng(19)
+    B, T, Tmax = 2, A.ROW_BLOCK + 40, A.ROW_BLOCK + 100
+    q, ck, cv, _ = _tiny_case(rng, B=B, T=T, Tmax=Tmax)
+    start = np.array([0, 60])
+    valid = np.array([T, T - 50])
+    full = A.attention(q, ck, cv, start, valid)
+    for b, i0, i1 in ((0, 0, 8), (1, A.ROW_BLOCK - 5, A.ROW_BLOCK + 7), (1, T - 3, T)):
+        got = A.attention_block(q, ck, cv, start, valid, T, b, i0, i1)
+        assert np.array_equal(got, full[b, i0:i1]), (b, i0, i1)

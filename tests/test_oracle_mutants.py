@@ -123,8 +123,15 @@ MUTANTS = [
     ("decode_at_kv_len", A, "decode", [("kv_len - 1, None, mode", "kv_len, None, mode")]),
     ("row_block_skips_its_last_row", A, "attention",
      [("np.arange(i0, min(T, i0 + ROW_BLOCK))", "np.arange(i0, min(T, i0 + ROW_BLOCK - 1))")]),
+    ("block_ignores_start", A, "attention_block", [("s, n = int(start[b]), int(valid[b])", "s, n = 0, int(valid[b])")]),
+    ("block_head_modulo", A, "attention_block", [("g = h // group", "g = h % (n_q // group)")]),
     ("rows_ignore_start", A, "attention_rows", [("s, nv = int(start[b]), int(valid[b])", "s, nv = 0, int(valid[b])")]),
     ("group_is_kv_head_count", A, "_kv_heads", [("return n_q, n_q // n_kv", "return n_q, n_kv")]),
+    # the pages' dtype chain (diagnostic mode)
+    ("chain_logits_in_bf16", A, "_attend_chain",
+     [("logits = (q @ K.T).astype(np.float32)", "logits = bf16.to_f32(bf16.from_f64(q @ K.T))")]),
+    ("chain_weights_not_rounded_to_bf16", A, "_attend_chain",
+     [("w = bf16.to_f64(bf16.from_f32(w))", "w = w.astype(np.float64)")]),
     # projections
     ("k_and_v_columns_swapped", P, "qkv_projection",
      [("k = y[..., nq:nq + nk].reshape(B, T, N_KV_HEADS, HEAD_DIM)\n    v = y[..., nq + nk:]",
