@@ -44,6 +44,8 @@ EXPORTS = (
     "grok_rope_kv_append",
     "grok_rope_cos_sin",
     "grok_attn_prefill",
+    "grok_attn_prefill_workspace",
+    "grok_attn_prefill_ws",
     "grok_attn_decode_workspace",
     "grok_attn_decode",
     "grok_attn_combine",
@@ -99,6 +101,10 @@ def load() -> ctypes.CDLL:
     lib.grok_rope_cos_sin.argtypes = [I, I, P, P, P]
     lib.grok_attn_prefill.restype = I
     lib.grok_attn_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
+    lib.grok_attn_prefill_workspace.restype = I
+    lib.grok_attn_prefill_workspace.argtypes = [I, I, ctypes.POINTER(S)]
+    lib.grok_attn_prefill_ws.restype = I
+    lib.grok_attn_prefill_ws.argtypes = [P, P, P, P, P, I, I, I, P, P, S, P, P]
     lib.grok_attn_decode_workspace.restype = I
     lib.grok_attn_decode_workspace.argtypes = [I, I, ctypes.POINTER(S), ctypes.POINTER(I)]
     lib.grok_attn_decode.restype = I
@@ -221,6 +227,36 @@ def prefill(q_rot, cache_k, cache_v, start_pos, valid_len, out, dev_status=None,
         _want(dev_status, "dev_status", torch.int32, (1,))
     _check(load().grok_attn_prefill(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(start_pos), _ptr(valid_len),
                                     B, T, Tmax, _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def prefill_workspace(B: int, Tmax: int) -> int:
+    """Bytes of the workspace prefill_ws() needs (fp16 copy of V and per-sequence flags)."""
+    n = ctypes.c_size_t(0)
+    _check(load().grok_attn_prefill_workspace(B, Tmax, ctypes.byref(n)))
+    return n.value
+
+
+def alloc_prefill_workspace(B: int, Tmax: int, device=None) -> torch.Tensor:
+    return torch.empty(prefill_workspace(B, Tmax), dtype=torch.uint8, device=device or "cuda")
+
+
+def prefill_ws(q_rot, cache_k, cache_v, start_pos, valid_len, out, workspace, dev_status=None, stream=None) -> None:
+    """prefill() with fp16 softmax weights and an fp16 copy of V in `workspace` (uint8 CUDA tensor)."""
+    B, T = q_rot.shape[0], q_rot.shape[1]
+    Tmax = cache_k.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    if valid_len is not None:
+        _want(valid_len, "valid_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(workspace, "workspace", torch.uint8, (workspace.numel(),))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_attn_prefill_ws(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(start_pos),
+                                       _ptr(valid_len), B, T, Tmax, _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _ptr(dev_status), _stream(stream)))
 
 
 def decode_workspace(B: int, Tmax: int) -> tuple[int, int]:

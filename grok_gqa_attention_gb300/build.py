@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libgrok_attn.so")
-SOURCES = ["abi.cu", "rope_append.cu", "prefill.cu", "decode.cu", "selftest.cu", "pipe.cu", "qkv.cu", "slots.cu"]
+SOURCES = ["abi.cu", "rope_append.cu", "prefill.cu", "decode.cu", "selftest.cu", "pipe.cu", "qkv.cu", "slots.cu", "int8_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

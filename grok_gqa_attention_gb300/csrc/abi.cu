@@ -94,18 +94,43 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-grok_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
-                                const uint64_t strides[3], const uint32_t box[4]) {
+static grok_status encode_tmap_16bit_4d(CUtensorMapDataType type, CUtensorMap* map, const void* base,
+                                       const uint64_t dims[4], const uint64_t strides[3], const uint32_t box[4]) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(GROK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
   cuuint64_t gstr[3] = {strides[0], strides[1], strides[2]};
   cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
+  CUresult r = fn(map, type, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GROK_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+  return GROK_OK;
+}
+
+grok_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                                const uint64_t strides[3], const uint32_t box[4]) {
+  return encode_tmap_16bit_4d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, dims, strides, box);
+}
+
+grok_status encode_tmap_f16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                               const uint64_t strides[3], const uint32_t box[4]) {
+  return encode_tmap_16bit_4d(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, map, base, dims, strides, box);
+}
+
+grok_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, const uint64_t dims[2], uint64_t row_stride,
+                              const uint32_t box[2]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(GROK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t gdim[2] = {dims[0], dims[1]};
+  cuuint64_t gstr[1] = {row_stride};
+  cuuint32_t bdim[2] = {box[0], box[1]};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstr, bdim, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GROK_ERR_CUDA, "cuTensorMapEncodeTiled (uint8) failed (CUresult %d)", int(r));
   return GROK_OK;
 }
 

@@ -37,5 +37,18 @@ grok_status check_launch(const char* what);
 // dims innermost first; strides in bytes for dims 1..3.
 grok_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                                 const uint64_t strides[3], const uint32_t box[4]);
+// The same for fp16 elements.
+grok_status encode_tmap_f16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                               const uint64_t strides[3], const uint32_t box[4]);
+
+// 2-D uint8 tensor map (dims innermost first, row stride in bytes), no
+// swizzle, zero fill out of bounds.
+grok_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, const uint64_t dims[2], uint64_t row_stride,
+                              const uint32_t box[2]);
+
+// Small-M int8 weight-only Linear (int8_small.cu): shape rule and launch.
+bool small_int8_ok(int M, int K, int N);
+grok_status linear_int8_small(const grok_bf16* x, const int8_t* w8, const float* scales, int M, int K, int N,
+                              grok_bf16* y, int32_t* dev_status, void* stream);
 
 }  // namespace grok

@@ -51,6 +51,20 @@
 // Keys beyond the last visible row of an item's final tile may hold anything
 // (including NaN): the softmax gives them weight 0 by selection and the softmax
 // warps zero those rows of the staged V tile before the PV product reads it.
+//
+// fp16 mode (kF16, grok_attn_prefill_ws): P is rounded once to fp16 (11-bit
+// significand, enough for the weights' precision) and P V is one product per
+// 16 keys instead of two, with V read as fp16 from a copy in the caller's
+// workspace (both operands of a kind::f16 product have one type). fp16's
+// exponent range cannot hold weights relative to the fixed reference 30, so
+// each row takes its own reference from its item's first key tile: the two
+// warps of a quadrant exchange their 64-key maxima once per item, and
+// m = 30 log2(e) tanh(y_max) + 8 (log2 units) puts the row's largest weight of
+// that tile at 2^-8. Later tiles whose logits rise above it by up to 2^24
+// (about 16.6 on the capped-logit scale) still fit fp16; a row whose weight sum
+// reaches 65504 (or any non-finite sum) puts its item on a fallback list in the
+// workspace, and so does every item of a sequence whose V does not fit fp16.
+// The bf16 mode of this kernel then recomputes exactly the listed items.
 #include "common.cuh"
 #include "host.cuh"
 
@@ -65,6 +79,7 @@ constexpr int kQBytes = 2 * 2 * kBox;       // two heads, two 64-wide halves of 
 constexpr int kTileBytes = 2 * kBox;        // one K or V tile: two 64-wide halves of d
 constexpr int kPfData = kQBytes + 2 * kPfStages * kTileBytes;
 constexpr int kPfSeqCache = 512;  // sequences whose start / valid length are staged in shared memory
+constexpr float kPfHeadroom = 8.0f;  // fp16 mode: log2 gap between a row's reference and its first-tile maximum
 
 struct PfBars {
   uint64_t q_full, q_empty;
@@ -73,8 +88,10 @@ struct PfBars {
   uint64_t mma_done;
   uint64_t lsum_ready[2];  // both halves of a slot posted their partial row sums
   uint64_t epi_done[2];    // the slot's eight epilogue warps' output stores have read their staging
+  uint64_t xbar[2][4];     // fp16 mode: [slot][quad] both warps of a quadrant posted their first-tile maxima
+  float xmax[2][4][2][32];   // [slot][quad][half][lane]
   float lsum[2][2][2][128];  // [item parity][slot][half][row]
-  int seq_start[kPfSeqCache], seq_valid[kPfSeqCache];
+  int seq_start[kPfSeqCache], seq_valid[kPfSeqCache], seq_vflag[kPfSeqCache];
   uint32_t tmem_base;
   int abort;
 };
@@ -86,6 +103,14 @@ struct PfParams {
   const int32_t* start_pos;
   const int32_t* valid_len;
   int32_t* status;
+  // fp16 mode: per-sequence "V does not fit fp16" flags and the fallback list it appends to
+  const int32_t* v_flags;
+  int32_t* fb_count;
+  int32_t* fb_list;
+  int fb_cap;
+  // bf16 mode over a list of items only (the fallback pass): item_list[0 .. *item_count)
+  const int32_t* item_list;
+  const int32_t* item_count;
 };
 
 struct PfItem {
@@ -95,17 +120,24 @@ struct PfItem {
   int n_kv;     // key tiles to visit (0: skip the item)
   int n_sub;    // 64-key halves of those tiles that hold a visible key
   int bad;      // GROK_DEV_* bits when the sequence's integers are invalid
+  bool redirect;  // fp16 mode: the sequence's V does not fit fp16; the fallback pass computes the item
 };
 
 // The item a CTA takes in round rd (-1 when there is none): rounds of gridDim.x
 // items, odd rounds in reverse CTA order, so the heavy items of one round and
 // the light items of the next land on the same CTA.
+template <bool kList>
 __device__ __forceinline__ int pf_item_index(const PfParams& p, int rd) {
   const int k = (rd & 1) ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
-  const long long item = (long long)rd * gridDim.x + k;
-  return item < p.n_items ? int(item) : -1;
+  const long long idx = (long long)rd * gridDim.x + k;
+  if (kList) {
+    const int n = min(__ldg(p.item_count), p.fb_cap);
+    return idx < n ? __ldg(p.item_list + idx) : -1;
+  }
+  return idx < p.n_items ? int(idx) : -1;
 }
 
+template <bool kF16>
 __device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars, int item) {
   PfItem it;
   it.hp = item % 3;
@@ -114,17 +146,28 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars,
   rest /= kKVHeads;
   it.b = rest % p.B;
   it.qt = p.n_qt - 1 - rest / p.B;  // heaviest (last) query tiles first
+  int vflag = 0;
   if (it.b < kPfSeqCache) {
     it.s = bars->seq_start[it.b];
     it.n = bars->seq_valid[it.b];
+    if (kF16) vflag = bars->seq_vflag[it.b];
   } else {
     it.s = __ldg(p.start_pos + it.b);
     it.n = p.valid_len ? __ldg(p.valid_len + it.b) : p.T;
+    if (kF16) vflag = __ldg(p.v_flags + it.b);
   }
   it.bad = 0;
+  it.redirect = false;
   if (it.s < 0 || (long long)it.s + p.T > p.Tmax) it.bad |= GROK_DEV_BAD_START;
   if (it.n < 1 || it.n > p.T) it.bad |= GROK_DEV_BAD_VALID;
   if (it.bad) {
+    it.kv_end = 0;
+    it.n_kv = 0;
+    it.n_sub = 0;
+    return it;
+  }
+  if (kF16 && vflag) {
+    it.redirect = true;
     it.kv_end = 0;
     it.n_kv = 0;
     it.n_sub = 0;
@@ -135,6 +178,18 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars,
   it.n_sub = (it.kv_end + 63) / 64;
   it.n_kv = (it.n_sub + 1) / 2;
   return it;
+}
+
+// Append an item to the fallback list (duplicates are harmless: the fallback
+// pass would compute the same bits twice).
+__device__ __forceinline__ void pf_fallback(const PfParams& p, int item) {
+  const int k = atomicAdd(p.fb_count, 1);
+  if (k < p.fb_cap) p.fb_list[k] = item;
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, int b_mn_major) {
+  return (1u << 4) | (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // MMA issue. The issuing thread shares its SMSP with busy softmax warps, so the
@@ -163,16 +218,18 @@ __device__ __forceinline__ void pf_issue_qk_half(uint32_t d, uint64_t qdesc, uin
   }
 }
 
-// O (+)= P V over the keys 64h .. 64h+63 of a tile.
+// O (+)= P V over the keys 64h .. 64h+63 of a tile: P as bf16 hi + lo (two
+// products per 16 keys), or, in fp16 mode, P and V fp16 (one product).
+template <bool kF16>
 __device__ __forceinline__ void pf_issue_pv_half(uint32_t d, uint32_t pbase, uint64_t vdesc, int h, bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_bf16(kPfRows, kD, 1);
+  constexpr uint32_t idesc = kF16 ? make_idesc_f16(kPfRows, kD, 1) : make_idesc_bf16(kPfRows, kD, 1);
 #pragma unroll
   for (int k4 = 0; k4 < 4; ++k4) {
     const int kk = 4 * h + k4;
     const uint32_t pcol = (kk >> 1) * 32 + (kk & 1) * 8;
     const uint64_t b = vdesc + uint64_t((kk * 2048) >> 4);
     umma_ts(d, pbase + pcol, b, idesc, (accumulate || k4 > 0) ? 1u : 0u);
-    umma_ts(d, pbase + pcol + 16, b, idesc, 1u);
+    if (!kF16) umma_ts(d, pbase + pcol + 16, b, idesc, 1u);
   }
 }
 
@@ -181,16 +238,17 @@ __device__ __forceinline__ void pf_issue_pv_half(uint32_t d, uint32_t pbase, uin
 constexpr uint32_t kPolyPairs = 0x3333;
 
 // S -> P for one 32-key chunk c of one row (this thread's TMEM lane): weights
-// exp(capped logit - 30), zero where masked, accumulated into the row sum and
-// returned as bf16 hi/lo halves for the caller to write back over S (keys
-// 32c..32c+31: hi in columns 32c..32c+15, lo in 32c+16..32c+31).
-template <bool kMask>
-__device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c, int rel, float& l0, float& l1,
-                                                 uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+// 2^(30 log2(e) tanh(y) - mref) (mref = 30 log2(e): exp(capped logit - 30)),
+// zero where masked, accumulated into the row sum and returned as bf16 hi/lo
+// halves for the caller to write back over S (keys 32c..32c+31: hi in columns
+// 32c..32c+15, lo in 32c+16..32c+31), or in fp16 mode as fp16 pairs (hi only).
+template <bool kMask, bool kF16>
+__device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c, int rel, float mref, float& l0,
+                                                 float& l1, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
   // The arithmetic of capped_weight and split_bf16x2, two columns at a time
   // with packed f32x2 instructions; the exp2 of the pairs in kPolyPairs is the
   // FMA-pipe polynomial instead of ex2.approx.
-  const uint64_t y2 = f2_pack(kY, kY), t2 = f2_pack(kT, kT), mt2 = f2_pack(-kT, -kT);
+  const uint64_t y2 = f2_pack(kY, kY), t2 = f2_pack(kT, kT), mt2 = f2_pack(-mref, -mref);
   uint64_t l = f2_pack(l0, l1);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
@@ -211,18 +269,32 @@ __device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c
     }
     const uint64_t w = f2_pack(w0, w1);
     l = f2_add(l, w);
-    hi[e] = pack_bf16x2(w0, w1);
-    float r0, r1;
-    f2_unpack(f2_sub(w, f2_pack(bf16lo_to_f32(hi[e]), bf16hi_to_f32(hi[e]))), r0, r1);
-    lo[e] = pack_bf16x2(r0, r1);
+    if (kF16) {
+      hi[e] = pack_f16x2(w0, w1);
+    } else {
+      hi[e] = pack_bf16x2(w0, w1);
+      float r0, r1;
+      f2_unpack(f2_sub(w, f2_pack(bf16lo_to_f32(hi[e]), bf16hi_to_f32(hi[e]))), r0, r1);
+      lo[e] = pack_bf16x2(r0, r1);
+    }
   }
   f2_unpack(l, l0, l1);
 }
 
+// Largest raw logit among this thread's visible keys of 32 logits starting at
+// key column c0 of the tile (-inf if none).
+template <bool kMask>
+__device__ __forceinline__ float pf_rowmax32(const uint32_t (&a)[32], int c0, int rel) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) mx = (!kMask || c0 + e <= rel) ? fmaxf(mx, __uint_as_float(a[e])) : mx;
+  return mx;
+}
+
 // One warp's half of a tile: key columns 64 half .. 64 half + 63 of its rows,
 // in two 32-column chunks (a TMEM load returns in ~30 cycles, so no prefetch).
-template <bool kMask>
-__device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel, float& l0, float& l1) {
+template <bool kMask, bool kF16>
+__device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel, float mref, float& l0, float& l1) {
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const int c = 2 * half + cc;
@@ -230,17 +302,37 @@ __device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel
     uint32_t hi[16], lo[16];
     tmem_ld32(trow + c * 32, a);
     tmem_wait_ld_dep(a);
-    pf_softmax_chunk<kMask>(a, c, rel, l0, l1, hi, lo);
+    pf_softmax_chunk<kMask, kF16>(a, c, rel, mref, l0, l1, hi, lo);
     tmem_st16(trow + c * 32, hi);
-    tmem_st16(trow + c * 32 + 16, lo);
+    if (!kF16) tmem_st16(trow + c * 32 + 16, lo);
   }
 }
 
+// Largest raw logit among this thread's visible keys of the half's 64 (-inf if none).
+template <bool kMask>
+__device__ __forceinline__ float pf_rowmax_half(uint32_t trow, int half, int rel) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t a[32];
+    tmem_ld32(trow + (2 * half + cc) * 32, a);
+    tmem_wait_ld_dep(a);
+    mx = fmaxf(mx, pf_rowmax32<kMask>(a, (2 * half + cc) * 32, rel));
+  }
+  return mx;
+}
+
+// kF16: fp16 mode; kList: bf16 mode over the fallback list only.
+template <bool kF16, bool kList>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const PfParams p) {
+  // (tm_v: bf16 V of the cache, or in fp16 mode the fp16 copy of V in the workspace)
   extern __shared__ uint8_t smem_raw[];
+  // The fallback pass runs as a programmatic dependent of the fp16 pass: wait
+  // for that grid's writes (the list, the outputs it replaces). A no-op otherwise.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + kQBytes;                           // K ring
@@ -267,6 +359,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars->o_empty[s], 256);
       mbar_init(&bars->lsum_ready[s], 256);
       mbar_init(&bars->epi_done[s], 8);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->xbar[s][q], 64);
     }
     mbar_init(&bars->mma_done, 2);
     bars->abort = 0;
@@ -276,6 +369,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   for (int b = threadIdx.x; b < p.B && b < kPfSeqCache; b += blockDim.x) {
     bars->seq_start[b] = __ldg(p.start_pos + b);
     bars->seq_valid[b] = p.valid_len ? __ldg(p.valid_len + b) : p.T;
+    if (kF16) bars->seq_vflag[b] = __ldg(p.v_flags + b);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
@@ -296,8 +390,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int kv_it = 0, q_it = 0;
-      for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
-        const PfItem it = pf_item(p, bars, item);
+      for (int rd = 0, item; (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
+        const PfItem it = pf_item<kF16>(p, bars, item);
         if (it.n_kv == 0) continue;
         if (!mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort, p.status)) break;
         mbar_arrive_expect_tx(&bars->q_full, kQBytes);
@@ -351,8 +445,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int kv_it = 0, q_it = 0, item_it = 0;
     int pc0 = 0, pc1 = 0;  // P hand-overs consumed per half (p_full parity)
     bool ok = true;
-    for (int rd = 0, item; ok && (item = pf_item_index(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item(p, bars, item);
+    for (int rd = 0, item; ok && (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
+      const PfItem it = pf_item<kF16>(p, bars, item);
       if (it.n_kv == 0) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, q_it & 1, abort, p.status))) break;
       {
@@ -392,7 +486,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         if (h) ++pc1; else ++pc0;
         tc_fence_after();
-        if (leader) pf_issue_pv_half(o_tm, s_tm, vd + st * kStageDesc, h, u > 0);
+        if (leader) pf_issue_pv_half<kF16>(o_tm, s_tm, vd + st * kStageDesc, h, u > 0);
         __syncwarp();
         if (h == 1 && u + 1 < it.n_sub) {
           // inputs of the next tile's steps: its V and the K after it
@@ -436,16 +530,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // query row within the tile
     const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
-    int tile_cnt = 0, item_it = 0, sub_cnt = 0;
-    for (int rd = 0, item; (item = pf_item_index(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item(p, bars, item);
+    int tile_cnt = 0, item_it = 0, sub_cnt = 0, xch_cnt = 0;
+    for (int rd = 0, item; (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
+      const PfItem it = pf_item<kF16>(p, bars, item);
       if (it.n_kv == 0) {
         if (it.bad && slot == 0 && half == 0 && r == 0) report(p.status, it.bad);
+        if (kF16 && it.redirect && slot == 0 && half == 0 && r == 0) pf_fallback(p, item);
         continue;
       }
       const int i = it.qt * kPfRows + r;
       const int lim = min(it.s + i, it.s + it.n - 1);  // last visible key of this row
       float l0 = 0.f, l1 = 0.f;
+      float mref = kT;  // bf16 mode: the fixed reference logit 30 (30 log2(e) in log2 units)
       bool ok = true;
       for (int u = half; u < it.n_sub; u += 2) {
         const int j = u >> 1;
@@ -459,11 +555,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int rel = lim - j * kPfKeys;       // columns c <= rel are visible
         // The choice must be warp-uniform: the TMEM loads and stores inside
         // are warp-collective (.sync.aligned).
-        if (__all_sync(0xffffffffu, rel >= 64 * half + 63))
-          pf_softmax_half<false>(trow, half, rel, l0, l1);
+        const bool unmasked = __all_sync(0xffffffffu, rel >= 64 * half + 63);
+        if (kF16 && j == 0) {
+          // fp16 mode: the row's reference from the item's first tile (both halves)
+          float mx = unmasked ? pf_rowmax_half<false>(trow, half, rel) : pf_rowmax_half<true>(trow, half, rel);
+          if (it.n_sub >= 2) {
+            bars->xmax[slot][quad][half][lane] = mx;
+            mbar_arrive(&bars->xbar[slot][quad]);
+            const bool w = mbar_wait(&bars->xbar[slot][quad], xch_cnt & 1, abort, p.status);
+            ++xch_cnt;
+            if (!__all_sync(0xffffffffu, w)) {
+              ok = false;
+              break;
+            }
+            mx = fmaxf(mx, bars->xmax[slot][quad][half ^ 1][lane]);
+          }
+          mref = kT * tanh_approx(mx * kY) + kPfHeadroom;  // key 0 is visible: mx is finite
+        }
+        if (unmasked)
+          pf_softmax_half<false, kF16>(trow, half, rel, mref, l0, l1);
         else
-          pf_softmax_half<true>(trow, half, rel, l0, l1);
-        if (u == it.n_sub - 1) {
+          pf_softmax_half<true, kF16>(trow, half, rel, mref, l0, l1);
+        if (!kF16 && u == it.n_sub - 1) {
           // Zero the V rows of the last tile that lie beyond every visible key.
           // Both slots do it (same zeros) before handing over their P, since
           // each slot's PV product may be issued first.
@@ -500,7 +613,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
            mbar_wait(&bars->o_full[1], item_it & 1, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const float inv_l = 1.0f / (bars->lsum[item_it & 1][slot][0][r] + bars->lsum[item_it & 1][slot][1][r]);
+      const float lt = bars->lsum[item_it & 1][slot][0][r] + bars->lsum[item_it & 1][slot][1][r];
+      // fp16 mode: a weight sum that reached fp16's range means some weight may
+      // have overflowed: the fallback pass recomputes the item (a half-0 warp
+      // of each quadrant reports; duplicates are harmless)
+      if (kF16 && half == 0 && __any_sync(0xffffffffu, !(lt < 65504.0f)) && lane == 0) pf_fallback(p, item);
+      const float inv_l = 1.0f / lt;
       const int h = it.g * kGroup + it.hp * 2 + slot;
       const int st_last = (tile_cnt - 1) % kPfStages;
       uint8_t* stage = (slot == 0 ? sK : sV) + st_last * kTileBytes + half * kBox;
@@ -557,14 +675,62 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// fp16 mode pre-pass: the fp16 copy of V. For sequence b with a valid start s,
+// rows [0, s + T) of the cache are rounded to nearest fp16 and rows
+// [s + T, round_up(s + T, 128)) are zeroed, so every key tile the fp16 pass
+// reads is finite. A finite |v| >= 65520 (beyond fp16) sets v_flags[b]: the
+// fp16 pass then hands all of that sequence's items to the fallback pass.
+__global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict__ cache_v, const int32_t* start_pos,
+                                                        int T, int Tmax, int vh_rows, uint4* __restrict__ vh,
+                                                        int32_t* v_flags) {
+  const int b = blockIdx.y;
+  const int s = __ldg(start_pos + b);
+  if (s < 0 || (long long)s + T > Tmax) return;  // the attention passes skip this sequence
+  const int rows = s + T, rows_pad = min(vh_rows, (rows + kPfKeys - 1) / kPfKeys * kPfKeys);
+  constexpr int kChunks = kKVHeads * kD / 8;  // 16-byte chunks (8 values) per row
+  bool over = false;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)rows_pad * kChunks;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int row = int(e / kChunks), ch = int(e % kChunks);
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (row < rows) {
+      const uint4 in = __ldg(cache_v + ((size_t)b * Tmax + row) * kChunks + ch);
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = bf16lo_to_f32(w[q]), c = bf16hi_to_f32(w[q]);
+        over |= (fabsf(a) >= 65520.f && fabsf(a) != INFINITY) || (fabsf(c) >= 65520.f && fabsf(c) != INFINITY);
+        o[q] = pack_f16x2(a, c);
+      }
+      out = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    vh[((size_t)b * vh_rows + row) * kChunks + ch] = out;
+  }
+  if (__any_sync(0xffffffffu, over) && (threadIdx.x & 31) == 0) atomicOr(v_flags + b, 1);
+}
+
 }  // namespace grok
 
 using namespace grok;
 
+// Extra inputs of the fp16 mode and of the fallback pass.
+struct PfExtra {
+  bool f16 = false;                 // fp16 mode: v_half holds the fp16 copy of V, [B][vh_rows][8][128]
+  const void* v_half = nullptr;
+  int vh_rows = 0;
+  const int32_t* v_flags = nullptr;
+  int32_t* fb_count = nullptr;      // fallback list (written by the fp16 pass, read by the fallback pass)
+  int32_t* fb_list = nullptr;
+  int fb_cap = 0;
+  bool fallback = false;            // bf16 mode over the listed items only, launched as a dependent
+};
+
 static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
                                   uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* start_pos,
                                   const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out, int32_t* dev_status,
-                                  void* stream) {
+                                  void* stream, const PfExtra& ex = PfExtra()) {
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
@@ -582,7 +748,13 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
     const uint64_t dims[4] = {kD, kKVHeads, kv_rows, kv_seqs};
     const uint64_t strides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, kv_rows * kKVHeads * kD * 2};
     if ((st = encode_tmap_bf16_4d(&tk, k_src, dims, strides, box)) != GROK_OK) return st;
-    if ((st = encode_tmap_bf16_4d(&tv, v_src, dims, strides, box)) != GROK_OK) return st;
+    if (ex.f16) {
+      const uint64_t hdims[4] = {kD, kKVHeads, uint64_t(ex.vh_rows), uint64_t(B)};
+      const uint64_t hstrides[3] = {kD * 2, uint64_t(kKVHeads) * kD * 2, uint64_t(ex.vh_rows) * kKVHeads * kD * 2};
+      if ((st = encode_tmap_f16_4d(&tv, ex.v_half, hdims, hstrides, box)) != GROK_OK) return st;
+    } else if ((st = encode_tmap_bf16_4d(&tv, v_src, dims, strides, box)) != GROK_OK) {
+      return st;
+    }
   }
   PfParams prm;
   prm.B = B;
@@ -594,18 +766,42 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
   prm.start_pos = start_pos;
   prm.valid_len = valid_len;
   prm.status = dev_status;
+  prm.v_flags = ex.v_flags;
+  prm.fb_count = ex.fb_count;
+  prm.fb_list = ex.fb_list;
+  prm.fb_cap = ex.fb_cap;
+  prm.item_list = ex.fallback ? ex.fb_list : nullptr;
+  prm.item_count = ex.fallback ? ex.fb_count : nullptr;
 
-  static bool attr_set[kMaxDevices] = {};  // per device; idempotent: every thread would set the same value
+  static bool attr_set[kMaxDevices][3] = {};  // per device and kernel instance; idempotent
   int dev = 0;
   grok_status dst = device_index(&dev);
   if (dst != GROK_OK) return dst;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+  const int mode = ex.f16 ? 1 : ex.fallback ? 2 : 0;
+  auto kernel = mode == 1 ? prefill_kernel<true, false> : mode == 2 ? prefill_kernel<false, true>
+                                                                    : prefill_kernel<false, false>;
+  if (!attr_set[dev][mode]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set[dev] = true;
+    attr_set[dev][mode] = true;
   }
-  const int grid = prm.n_items < sms ? prm.n_items : sms;
-  prefill_kernel<<<grid, kPfThreads, kPfSmem, static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, prm);
+  // The fallback pass does not know how many items it has (the list is on the
+  // device), so it takes one CTA per SM; it is a programmatic dependent of the
+  // fp16 pass, so its launch overlaps that pass's tail, and it waits for the
+  // whole fp16 grid (griddepcontrol.wait) before reading the list.
+  const int grid = ex.fallback ? sms : (prm.n_items < sms ? prm.n_items : sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = kPfSmem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = ex.fallback ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, prm);
+  if (e != cudaSuccess) return fail(cuda_status(e), "prefill launch: %s", cudaGetErrorString(e));
   return check_launch("prefill");
 }
 
@@ -642,4 +838,86 @@ extern "C" grok_status grok_attn_prefill_paged(const grok_bf16* q_rot, const gro
   return prefill_launch(q_rot, k_pool, v_pool, uint64_t(n_pages) * GROK_PAGE_TOKENS, 1,
                         PageMap{block_table, max_pages, n_pages}, start_pos, valid_len, B, T, int(Tmax), out,
                         dev_status, stream);
+}
+
+// ----------------------------------------------------------------------------
+// Prefill with fp16 softmax weights (grok_attn_prefill_ws). Workspace layout:
+//   int32 v_flags[B], fb_count, fb_list[fb_cap]  (padded to 256 bytes)
+//   fp16 V copy [B][round_up(Tmax, 128)][8][128]
+static int ws_vh_rows(int Tmax) { return (Tmax + kPfKeys - 1) / kPfKeys * kPfKeys; }
+static int ws_fb_cap(int B, int Tmax) {
+  // items of the largest call (T = Tmax); each may be listed by up to 8
+  // quadrant warps of the fp16 pass plus once for its sequence's V
+  return 9 * ((Tmax + kPfRows - 1) / kPfRows) * B * kKVHeads * 3;
+}
+static size_t ws_header_bytes(int B, int Tmax) {
+  return ((size_t(B) + 1 + size_t(ws_fb_cap(B, Tmax))) * sizeof(int32_t) + 255) & ~size_t(255);
+}
+
+extern "C" grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes) {
+  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace: null pointer");
+  if (B < 1 || Tmax < 1 || Tmax > GROK_MAX_POSITION || (long long)B * ws_vh_rows(Tmax) > (1LL << 31))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace: need B >= 1, 1 <= Tmax <= %d",
+                GROK_MAX_POSITION);
+  *bytes = ws_header_bytes(B, Tmax) + size_t(B) * ws_vh_rows(Tmax) * kKVHeads * kD * 2;
+  return GROK_OK;
+}
+
+extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k,
+                                            const grok_bf16* cache_v, const int32_t* start_pos,
+                                            const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
+                                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                            void* stream) {
+  if (!q_rot || !cache_k || !cache_v || !start_pos || !out || !workspace)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: null pointer");
+  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: bf16 tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace must be 256-byte aligned");
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+                GROK_MAX_POSITION, B, T, Tmax);
+  size_t need = 0;
+  grok_status st = grok_attn_prefill_workspace(B, Tmax, &need);
+  if (st != GROK_OK) return st;
+  if (workspace_bytes < need)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, need);
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != GROK_OK) return st;
+  const int vh_rows = ws_vh_rows(Tmax);
+  int32_t* v_flags = static_cast<int32_t*>(workspace);
+  int32_t* fb_count = v_flags + B;
+  int32_t* fb_list = fb_count + 1;
+  void* vh = static_cast<char*>(workspace) + ws_header_bytes(B, Tmax);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e = cudaMemsetAsync(v_flags, 0, (size_t(B) + 1) * sizeof(int32_t), s);  // flags and list count
+  if (e != cudaSuccess) return fail(cuda_status(e), "cudaMemsetAsync: %s", cudaGetErrorString(e));
+  {
+    const long long per_seq = (long long)vh_rows * (kKVHeads * kD / 8);
+    long long bx = (per_seq + 255) / 256;
+    const long long cap = ((long long)sms * 8 + B - 1) / B;  // about 8 blocks per SM in all
+    if (bx > cap) bx = cap;
+    if (bx < 1) bx = 1;
+    v_to_half_kernel<<<dim3(unsigned(bx), unsigned(B)), 256, 0, s>>>(reinterpret_cast<const uint4*>(cache_v),
+                                                                     start_pos, T, Tmax, vh_rows,
+                                                                     static_cast<uint4*>(vh), v_flags);
+    if ((st = check_launch("v_to_half")) != GROK_OK) return st;
+  }
+  PfExtra ex;
+  ex.f16 = true;
+  ex.v_half = vh;
+  ex.vh_rows = vh_rows;
+  ex.v_flags = v_flags;
+  ex.fb_count = fb_count;
+  ex.fb_list = fb_list;
+  ex.fb_cap = ws_fb_cap(B, Tmax);
+  if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                           valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
+    return st;
+  ex.f16 = false;
+  ex.fallback = true;
+  return prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                        valid_len, B, T, Tmax, out, dev_status, stream, ex);
 }

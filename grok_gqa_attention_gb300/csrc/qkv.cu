@@ -444,164 +444,6 @@ __global__ void __launch_bounds__(kDqThreads) dequant_int8_kernel(const uint4* _
   }
 }
 
-// ----------------------------------------------------------------------------
-// Small-M int8 Linear (decode-sized batches, M <= 32): y = x . dequant(w8, s)
-// without writing the bf16 weight out. The int8 weight is read once; each
-// element is dequantized exactly as grok_dequant_int8 does it (fp32 product,
-// rounded to bf16) into a shared-memory tile and multiplied there.
-//   grid: one CTA per 64 output columns; 8 warps, warp w takes the K rows
-//   [w K/8, (w+1) K/8) in steps of 16. Per step a lane holds one 32-column
-//   half of one row (2 x 16 bytes, four steps in flight), dequantizes it with
-//   the column scales it keeps in registers, and stores it to the warp's
-//   16 x 64 bf16 tile (rows padded to 144 bytes: 16-byte aligned and free of
-//   bank conflicts for ldmatrix). ldmatrix.trans gives the B fragments of the
-//   eight 8-column tiles; x supplies A (rows >= M read as zero); mma.sync
-//   m16n8k16 accumulates in fp32. The eight warps' partial sums are added in
-//   a fixed order through shared memory and rounded to bf16.
-// Memory-bound on the weight: 1 byte per weight element.
-constexpr int kSmThreads = 256;
-constexpr int kSmWarps = kSmThreads / 32;
-constexpr int kSmCols = 64;       // output columns per CTA
-constexpr int kSmPre = 4;         // 16-row steps in flight per warp
-constexpr int kSmRowBytes = 144;  // staging row: 64 bf16 + 16 bytes of padding
-constexpr int kSmMaxM = 32;
-
-constexpr int small_smem_bytes(int mt) { return kSmWarps * 16 * kSmRowBytes + kSmWarps * mt * 16 * kSmCols * 4; }
-
-template <int MT>
-__global__ void __launch_bounds__(kSmThreads) linear_int8_small_kernel(const uint32_t* __restrict__ x,
-                                                                       const uint4* __restrict__ w8,
-                                                                       const float4* __restrict__ scales, int M,
-                                                                       int K, int N, uint32_t* __restrict__ y) {
-  extern __shared__ __align__(16) uint8_t sm_small[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kSmCols;
-  uint8_t* tile = sm_small + warp * 16 * kSmRowBytes;
-  float* red = reinterpret_cast<float*>(sm_small + kSmWarps * 16 * kSmRowBytes);
-  const int drow = lane >> 1, dcol = (lane & 1) * 32;  // this lane's row and 32 columns of a step
-  float sc[32];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 v = __ldg(scales + (n0 + dcol) / 4 + q);
-    sc[4 * q] = v.x, sc[4 * q + 1] = v.y, sc[4 * q + 2] = v.z, sc[4 * q + 3] = v.w;
-  }
-  const int steps = K / (16 * kSmWarps);  // multiple of kSmPre (host check)
-  const int kw = warp * steps * 16;
-  const size_t row_u4 = size_t(N) / 16;
-  const size_t col_u4 = size_t(n0 + dcol) / 16;
-  uint4 raw[kSmPre][2];
-#pragma unroll
-  for (int j = 0; j < kSmPre; ++j) {
-    const size_t off = size_t(kw + j * 16 + drow) * row_u4 + col_u4;
-    raw[j][0] = __ldg(w8 + off);
-    raw[j][1] = __ldg(w8 + off + 1);
-  }
-  float acc[MT][8][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-  const int g = lane >> 2, t = lane & 3;
-  const int mi = lane >> 3, mr = lane & 7;
-  const uint32_t tile_s = smem_u32(tile);
-  for (int i0 = 0; i0 < steps; i0 += kSmPre) {
-#pragma unroll
-    for (int j = 0; j < kSmPre; ++j) {
-      const int i = i0 + j;
-      const int k0 = kw + i * 16;
-      const uint4 c0 = raw[j][0], c1 = raw[j][1];
-      if (i + kSmPre < steps) {  // refill this slot with the step kSmPre ahead
-        const size_t off = size_t(k0 + kSmPre * 16 + drow) * row_u4 + col_u4;
-        raw[j][0] = __ldg(w8 + off);
-        raw[j][1] = __ldg(w8 + off + 1);
-      }
-      // A fragments of x for rows mt*16 + g (+8), K columns k0 + 2t (+8)
-      uint32_t a[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const int r0 = mt * 16 + g, r1 = r0 + 8;
-        const size_t b0 = (size_t(r0) * K + k0) / 2 + t, b1 = (size_t(r1) * K + k0) / 2 + t;
-        a[mt][0] = r0 < M ? __ldg(x + b0) : 0u;
-        a[mt][1] = r1 < M ? __ldg(x + b1) : 0u;
-        a[mt][2] = r0 < M ? __ldg(x + b0 + 4) : 0u;
-        a[mt][3] = r1 < M ? __ldg(x + b1 + 4) : 0u;
-      }
-      // dequantize this lane's 32 weights into the warp's tile
-      const uint32_t word[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      uint32_t pk[16];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float f[4];
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          const int v = int(word[q] << (24 - 8 * bb)) >> 24;  // sign-extended byte bb
-          f[bb] = __fmul_rn(float(v), sc[4 * q + bb]);
-        }
-        pk[2 * q] = pack_bf16x2(f[0], f[1]);
-        pk[2 * q + 1] = pack_bf16x2(f[2], f[3]);
-      }
-      __syncwarp();  // the previous step's ldmatrix reads of the tile are done
-      uint4* dst = reinterpret_cast<uint4*>(tile + drow * kSmRowBytes + dcol * 2);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      __syncwarp();
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {  // pairs of 8-column tiles
-        const int row = (mi & 1) * 8 + mr, col = np * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tile_s + row * kSmRowBytes + col * 2, b0, b1, b2, b3);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16_16816(acc[mt][2 * np], a[mt], b0, b1);
-          mma_bf16_16816(acc[mt][2 * np + 1], a[mt], b2, b3);
-        }
-      }
-    }
-  }
-  // partial sums: acc[mt][nt] holds rows mt*16 + g (+8) and columns nt*8 + 2t (+1)
-  float* mine = red + warp * (MT * 16 * kSmCols);
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mine[(mt * 16 + g + 8 * (e >> 1)) * kSmCols + nt * 8 + 2 * t + (e & 1)] = acc[mt][nt][e];
-  __syncthreads();
-  for (int o = threadIdx.x; o < MT * 16 * kSmCols / 2; o += kSmThreads) {  // pairs of columns
-    const int row = (2 * o) / kSmCols, col = (2 * o) % kSmCols;
-    if (row >= M) continue;
-    float v0 = 0.f, v1 = 0.f;
-    for (int w = 0; w < kSmWarps; ++w) {  // fixed order: the result does not depend on scheduling
-      v0 += red[w * (MT * 16 * kSmCols) + row * kSmCols + col];
-      v1 += red[w * (MT * 16 * kSmCols) + row * kSmCols + col + 1];
-    }
-    y[(size_t(row) * N + n0 + col) / 2] = pack_bf16x2(v0, v1);
-  }
-}
-
-static bool small_int8_ok(int M, int K, int N) {
-  return M >= 1 && M <= kSmMaxM && K % (16 * kSmWarps * kSmPre) == 0 && N % kSmCols == 0;
-}
-
-static grok_status linear_int8_small(const grok_bf16* x, const int8_t* w8, const float* scales, int M, int K, int N,
-                                     grok_bf16* y, void* stream) {
-  const int mt = M <= 16 ? 1 : 2;
-  const int smem = small_smem_bytes(mt);
-  static bool attr_set[kMaxDevices][2] = {};  // per device and instance; idempotent
-  int dev = 0;
-  grok_status st = device_index(&dev);
-  if (st != GROK_OK) return st;
-  auto kernel = mt == 1 ? linear_int8_small_kernel<1> : linear_int8_small_kernel<2>;
-  if (!attr_set[dev][mt - 1]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set[dev][mt - 1] = true;
-  }
-  kernel<<<unsigned(N / kSmCols), kSmThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint32_t*>(x), reinterpret_cast<const uint4*>(w8), reinterpret_cast<const float4*>(scales),
-      M, K, N, reinterpret_cast<uint32_t*>(y));
-  return check_launch("linear_int8_small");
-}
 
 grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, int K, int N, QkvParams& prm,
                        void* stream) {
@@ -810,7 +652,8 @@ extern "C" grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, co
     return fail(GROK_ERR_INVALID_ARG,
                 "grok_linear_int8: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)",
                 kQkvBK, kQkvBN, M, K, N);
-  // Decode-sized M: one pass over the int8 weight, dequantized in shared memory.
+  // Decode-sized M: one pass over the int8 weight, dequantized in shared memory
+  // (int8_small.cu).
   if (small_int8_ok(M, K, N)) {
     if (!x || !w8 || !scales) return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: null pointer");
     if (!aligned16(x) || !aligned16(w8) || !aligned16(scales))
@@ -818,7 +661,7 @@ extern "C" grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, co
     int sms = 0;
     grok_status st0 = device_sm_count(&sms);
     if (st0 != GROK_OK) return st0;
-    return linear_int8_small(x, w8, scales, M, K, N, y, stream);
+    return linear_int8_small(x, w8, scales, M, K, N, y, dev_status, stream);
   }
   grok_bf16* w16 = static_cast<grok_bf16*>(workspace);
   grok_status st = grok_dequant_int8(w8, scales, K, N, w16, stream);

@@ -18,6 +18,7 @@
  *
  * Calls by group:
  *   attention core      grok_rope_kv_append, grok_rope_cos_sin, grok_attn_prefill,
+ *                       grok_attn_prefill_workspace, grok_attn_prefill_ws,
  *                       grok_attn_decode_workspace, grok_attn_decode, grok_attn_combine,
  *                       grok_attn_decode_step_static, grok_attn_decode_step(_workspace)
  *   projections         grok_qkv_project, grok_linear, grok_dequant_int8,
@@ -158,6 +159,32 @@ grok_status grok_rope_cos_sin(int first_position, int n_positions, float* cos_ou
 grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
                               const int32_t* start_pos, const int32_t* valid_len, int B, int T, int Tmax,
                               grok_bf16* out, int32_t* dev_status, void* stream);
+
+/*
+ * Prefill with fp16 softmax weights (same operation, arguments and results as
+ * grok_attn_prefill; ch. 4 §4.5.3 casts the softmax weights to the value dtype
+ * before the weighted sum, which this call does in fp16 instead of bf16, so
+ * each P V product runs once instead of twice). Each row's weights are taken
+ * relative to a reference set from its first key tile (its largest weight
+ * there is 2^-8) and rounded once to fp16; V is read from an fp16 copy that
+ * the call first writes into `workspace` (rows [0, start_pos[b] + T) of each
+ * sequence rounded to nearest fp16, then zeros to the next multiple of 128).
+ * Items (128 query rows x 2 heads) whose weights could leave fp16's range (a
+ * row's weight sum reaching 65504), and every item of a sequence holding a
+ * finite |v| >= 65520, are listed in the workspace and recomputed by a second
+ * pass with bf16 weights from the bf16 cache, so every finite input is
+ * handled; results then equal grok_attn_prefill's for those items.
+ *   workspace: caller-owned device memory, 256-byte aligned, of at least
+ *   grok_attn_prefill_workspace(B, Tmax) bytes (B * round_up(Tmax, 128) * 2 KB
+ *   for the V copy plus a header of about B * Tmax / 128 * 864 bytes); it holds
+ *   nothing between calls, and calls that overlap on the GPU need separate
+ *   workspaces.
+ */
+grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes);
+grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
+                                 const int32_t* start_pos, const int32_t* valid_len, int B, int T, int Tmax,
+                                 grok_bf16* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 void* stream);
 
 /*
  * Bytes of device workspace grok_attn_decode needs for B sequences and a cache
@@ -316,9 +343,11 @@ grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, in
  *   grok_linear (so K % 64 == 0, N % 256 == 0). For prefill-sized M the
  *   product is tensor-bound and the one pass over the weight costs a few
  *   percent; the workspace may be reused across calls with the same weight.
- *   For decode-sized M (M <= 32, K a multiple of 512, N of 64) the weight is
- *   instead read once and dequantized on chip, the same per-element rounding,
- *   and the workspace is not touched (it must still be passed).
+ *   For decode-sized M (M <= 32, K a multiple of 512) the weight is instead
+ *   read once and dequantized on chip, the same per-element rounding: clusters
+ *   of 8 CTAs split K and add their partial sums in a fixed order, so the bits
+ *   do not depend on scheduling. The workspace is not touched then (it must
+ *   still be passed).
  * All pointers device-resident and 16-byte aligned; w16, the workspace and y
  * 32-byte aligned. Asynchronous on stream.
  */

@@ -33,7 +33,10 @@ def run_append(inp: W.Inputs, dev="cuda"):
     return q_rot, ck, cv, int(status.item())
 
 
-def run_prefill(inp: W.Inputs, dev="cuda"):
+PREFILL_IMPLS = ("bf16p", "f16p")  # grok_attn_prefill (P as bf16 hi + lo) and grok_attn_prefill_ws (fp16 P)
+
+
+def run_prefill(inp: W.Inputs, dev="cuda", impl="bf16p"):
     """Append then prefill on the GPU; returns (q_rot, cache_k, cache_v, out) bits and status."""
     import grok_gqa_attention_gb300 as G
     q_rot, ck, cv, st = run_append(inp, dev)
@@ -41,7 +44,11 @@ def run_prefill(inp: W.Inputs, dev="cuda"):
     valid = None if inp.valid_len is None else inp.valid_len.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(q_rot)
-    G.prefill(q_rot, ck, cv, start, valid, out, status)
+    if impl == "f16p":
+        ws = G.alloc_prefill_workspace(q_rot.shape[0], ck.shape[1], dev)
+        G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status)
+    else:
+        G.prefill(q_rot, ck, cv, start, valid, out, status)
     torch.cuda.synchronize()
     return (W.bits(q_rot.cpu()), W.bits(ck.cpu()), W.bits(cv.cpu()), W.bits(out.cpu()),
             st | int(status.item()))

@@ -1,10 +1,16 @@
-"""K2 parity: prefill attention against the exact fp64 oracle."""
+"""K2 parity: prefill attention against the exact fp64 oracle, for both prefill
+calls: grok_attn_prefill (softmax weights as bf16 hi + lo, no workspace) and
+grok_attn_prefill_ws (fp16 weights with a lazily moved row maximum, fp16 copy
+of V in a workspace, bf16 path for sequences whose V does not fit fp16)."""
+import functools
+
 import numpy as np
 import pytest
+import torch
 
 import workloads as W
 from oracle import attention as A
-from tests.gpu_util import cached_inputs, oracle_append, run_prefill
+from tests.gpu_util import PREFILL_IMPLS, cached_inputs, oracle_append, run_prefill
 from tests.parity_util import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -23,19 +29,20 @@ SMALL_CASES = {
 }
 
 
-def _full_check(inp, what):
-    oq, ok_, ov, out, status = run_prefill(inp)
+def _full_check(inp, what, impl):
+    oq, ok_, ov, out, status = run_prefill(inp, impl=impl)
     assert status == 0
     rq, rk, rv = oracle_append(inp)
     assert np.array_equal(oq, rq) and np.array_equal(ok_, rk) and np.array_equal(ov, rv)
     valid = None if inp.valid_len is None else inp.valid_len.numpy()
     ref = A.attention(rq, rk, rv, inp.start_pos.numpy(), valid)
-    return assert_close(out, ref, what)
+    return assert_close(out, ref, f"{what} [{impl}]")
 
 
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("case", list(SMALL_CASES))
-def test_prefill_matches_oracle_elementwise(case):
-    _full_check(SMALL_CASES[case](), case)
+def test_prefill_matches_oracle_elementwise(case, impl):
+    _full_check(SMALL_CASES[case](), case, impl)
 
 
 def _sample_rows(B, T, n, seed):
@@ -64,12 +71,18 @@ def _whole_tiles(name, inp):
     return [(b, i0) for b in (0, w.B - 1) for i0 in range(0, w.T, 128)]
 
 
+@functools.lru_cache(maxsize=1)
+def _oracle_append_cached(name):
+    return oracle_append(cached_inputs(name))
+
+
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("name", ["prefill_b1_t8192", "ragged_prefill_b8_t2048", "chunked_prefill_b4_t256_at6144"])
-def test_prefill_full_size_whole_tiles_and_sampled_rows(name):
+def test_prefill_full_size_whole_tiles_and_sampled_rows(name, impl):
     inp = cached_inputs(name)
-    oq, ok_, ov, out, status = run_prefill(inp)
+    oq, ok_, ov, out, status = run_prefill(inp, impl=impl)
     assert status == 0
-    rq, rk, rv = oracle_append(inp)
+    rq, rk, rv = _oracle_append_cached(name)
     assert np.array_equal(oq, rq) and np.array_equal(ok_, rk) and np.array_equal(ov, rv)
     w = inp.workload
     valid = None if inp.valid_len is None else inp.valid_len.numpy()
@@ -77,48 +90,94 @@ def test_prefill_full_size_whole_tiles_and_sampled_rows(name):
     for b, i0 in _whole_tiles(name, inp):
         i1 = min(i0 + 128, w.T)
         ref = A.attention_block(rq, rk, rv, start, valid, w.T, b, i0, i1)
-        assert_close(out[b, i0:i1], ref, f"{name} tile b={b} rows {i0}..{i1 - 1}")
+        assert_close(out[b, i0:i1], ref, f"{name} tile b={b} rows {i0}..{i1 - 1} [{impl}]")
     rows = _sample_rows(w.B, w.T, 160, seed=1)
     ref, _ = A.attention_rows(rq, rk, rv, start, valid, w.T, rows)
     got = np.stack([out[b, i, h] for (b, i, h) in rows])
-    assert_close(got, ref, name)
+    assert_close(got, ref, f"{name} [{impl}]")
     vals = W.from_bits(out).float()
     assert bool(vals.isfinite().all())
 
 
-def test_prefill_never_reads_rows_beyond_the_memory_mask():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_never_reads_rows_beyond_the_memory_mask(impl):
     """NaN in every cache row at or beyond start + T gives the same bits as finite junk."""
     a = W.custom(B=2, T=200, Tmax=512, start_pos=[100, 37], valid_len=[200, 150], seed=21, junk="finite")
     b = W.custom(B=2, T=200, Tmax=512, start_pos=[100, 37], valid_len=[200, 150], seed=21, junk="nan")
-    oa = run_prefill(a)[3]
-    ob = run_prefill(b)[3]
+    oa = run_prefill(a, impl=impl)[3]
+    ob = run_prefill(b, impl=impl)[3]
     assert np.array_equal(oa, ob)
 
 
-def test_prefill_saturated_logits():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_saturated_logits(impl):
     """Large inputs push |logits| far past the cap: weights span exp(-60)..1."""
     inp = W.custom(B=1, T=256, Tmax=256, start_pos=[0], seed=22, scale=12.0)
-    _full_check(inp, "saturated")
+    _full_check(inp, "saturated", impl)
 
 
-def test_prefill_all_weights_tiny():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_all_weights_tiny(impl):
     """Small inputs with all logits near zero: every weight near exp(-30) relative to the fixed reference."""
     inp = W.custom(B=1, T=192, Tmax=256, start_pos=[0], seed=23, scale=0.05)
-    _full_check(inp, "tiny logits")
+    _full_check(inp, "tiny logits", impl)
 
 
-def test_prefill_one_visible_key_copies_v():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_row_maximum_rises_across_tiles(impl):
+    """Keys of the first 128-key tile give logits near 0, later keys logits near +-30:
+    a row's maximum rises by up to ~43 octaves after its first tile, so the fp16
+    path must move its reference and rescale O and the row sum (more than once,
+    since the middle tile rises only part of the way)."""
+    inp = W.custom(B=1, T=400, Tmax=512, start_pos=[0], seed=26, scale=3.0)
+    k = inp.k.float()
+    k[:, :128] *= 0.02      # first tile: |logits| ~ 0.2 before the cap
+    k[:, 128:256] *= 0.7    # second tile: part of the way up
+    k[:, 256:] *= 4.0       # later tiles: saturated
+    inp.k.copy_(k.to(torch.bfloat16))
+    _full_check(inp, "rising maximum", impl)
+
+
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_values_beyond_fp16_range(impl):
+    """V values above fp16's largest finite value (65504) in one sequence: the fp16
+    path must run that sequence from the bf16 cache (the other sequence stays on
+    fp16), with results matching the oracle."""
+    inp = W.custom(B=2, T=300, Tmax=384, start_pos=[0, 20], valid_len=[300, 250], seed=27)
+    v = inp.v.float()
+    v[1, 5] *= 4e4           # |v| up to ~5e5 in sequence 1 (a visible row)
+    inp.v.copy_(v.to(torch.bfloat16))
+    assert float(inp.v[1].float().abs().max()) > 65504 and float(inp.v[0].float().abs().max()) < 65504
+    oq, ok_, ov, out, status = run_prefill(inp, impl=impl)
+    assert status == 0
+    rq, rk, rv = oracle_append(inp)
+    ref = A.attention(rq, rk, rv, inp.start_pos.numpy(), inp.valid_len.numpy())
+    # sequence 0 keeps the usual absolute tolerance
+    assert_close(out[0], ref[0], f"fp16-range sequence [{impl}]")
+    # sequence 1's outputs reach ~1e5 where the big row has weight: errors relative to
+    # each output row's scale (its largest |value|, at least 1)
+    g = W.from_bits(out[1]).float().numpy()
+    r = W.from_bits(ref[1]).float().numpy()
+    row_scale = np.maximum(1.0, np.abs(r).max(axis=-1, keepdims=True))
+    rel = np.abs(g - r) / row_scale
+    assert np.isfinite(g).all()
+    assert rel.max() <= 2.0 ** -7 and rel.mean() <= 1e-3, (float(rel.max()), float(rel.mean()))
+
+
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_one_visible_key_copies_v(impl):
     """valid_len = 1: every row sees only key 0, so the output is v[0] exactly."""
     inp = W.custom(B=1, T=64, Tmax=64, start_pos=[0], valid_len=[1], seed=24)
-    oq, ok_, ov, out, status = run_prefill(inp)
+    oq, ok_, ov, out, status = run_prefill(inp, impl=impl)
     assert status == 0
     want = np.repeat(ov[0, 0], 6, axis=0)     # [48, 128]: head h reads kv head h // 6
     for i in range(64):
         assert np.array_equal(out[0, i], want)
 
 
-def test_prefill_bad_integers_set_status():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_bad_integers_set_status(impl):
     import grok_gqa_attention_gb300 as G
     inp = W.custom(B=2, T=16, Tmax=32, start_pos=[0, 8], valid_len=[16, 0], seed=25)
-    *_, status = run_prefill(inp)
+    *_, status = run_prefill(inp, impl=impl)
     assert status & G.DEV_BAD_VALID
