@@ -3,7 +3,8 @@
 
 A step is one pass of the prefill hot path over the long causal prefill
 (B=1, T=8192, 48 query / 8 KV heads, d=128, bf16): RoPE + KV-cache append,
-then soft-capped causal GQA attention. `value` is algorithmic attention
+then soft-capped causal GQA attention (grok_attn_prefill_ws: fp16 softmax
+weights, fp16 copy of V in a workspace). `value` is algorithmic attention
 TFLOP/s (48 heads x visible keys x 4 x 128 FLOP per query row) over the whole
 step, inputs resident in HBM. The decode hot path (B=32, cached lengths uniform
 in [1, 8191]: append, split-K decode, combine) is measured in the same run and
@@ -245,15 +246,48 @@ class OraclePool:
         self.pool.join()
 
 
+def _oracle_c1_single_thread():
+    """The whole tiny causal prefill (B1, T128) through the oracle in one process with one
+    BLAS thread: the RoPE + append chain, then exact attention; seconds for each."""
+    import workloads as W
+    from oracle import attention as A
+    from oracle import rope as R
+    inp = W.generate("prefill_b1_t128")
+    t0 = time.perf_counter()
+    q_rot, ck, cv = R.rope_kv_append(W.bits(inp.q), W.bits(inp.k), W.bits(inp.v), inp.start_pos.numpy(),
+                                     W.bits(inp.cache_k), W.bits(inp.cache_v))
+    t1 = time.perf_counter()
+    A.attention(q_rot, ck, cv, inp.start_pos.numpy(), None)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
 def cpu_baseline(n_tokens: int = 512) -> dict:
     pool = OraclePool(PREFILL_WORKLOAD)
     try:
         r, wall, used = pool.rate(n_tokens, seed=0)
     finally:
         pool.close()
+    # the tiny causal prefill on one core (one spawned process, one BLAS thread)
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(1) as p1:
+            t_rope, t_attn = p1.apply(_oracle_c1_single_thread)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    c1_flops = prefill_flops(np.zeros(1, dtype=np.int64), None, 128)
     return {"value": r, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
             "sample": (f"{n_tokens} random query tokens x 48 heads of {PREFILL_WORKLOAD}, exact fp64 NumPy "
-                       f"oracle, attention only (RoPE/append precomputed), {wall:.1f} s on {used} cores")}
+                       f"oracle, attention only (RoPE/append precomputed), {wall:.1f} s on {used} cores"),
+            "c1_single_thread": {"workload": "prefill_b1_t128", "threads": 1, "rope_append_s": t_rope,
+                                 "attention_s": t_attn, "attention_TFLOP/s": c1_flops / t_attn / 1e12,
+                                 "algorithmic_gflop": c1_flops / 1e9}}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -280,6 +314,7 @@ def run_ours(args, rank: int, world: int, dist):
     q_rot = torch.empty_like(q)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pf_ws = G.alloc_prefill_workspace(B, Tmax, dev)
     flops = prefill_flops(inp.start_pos.numpy(), None if inp.valid_len is None else inp.valid_len.numpy(), T)
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -291,7 +326,7 @@ def run_ours(args, rank: int, world: int, dist):
         G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
         if e is not None:
             e[1].record(stream)
-        G.prefill(q_rot, ck, cv, start, valid, out, status)
+        G.prefill_ws(q_rot, ck, cv, start, valid, out, pf_ws, status)
         if e is not None:
             e[2].record(stream)
 
@@ -325,6 +360,22 @@ def run_ours(args, rank: int, world: int, dist):
     prefill_times = [e[1].elapsed_time(e[2]) for e in ev]
     ms_append = float(np.mean(append_times))
     ms_prefill = float(np.mean(prefill_times))
+    # context: the workspace-free prefill (softmax weights as bf16 hi + lo, two P V products)
+    out_b = torch.empty_like(out)
+    for _ in range(args.warmup):
+        G.prefill(q_rot, ck, cv, start, valid, out_b, status)
+    ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e in ev_b:
+        e[0].record(stream)
+        G.prefill(q_rot, ck, cv, start, valid, out_b, status)
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    bf16p_times = [a.elapsed_time(b_) for a, b_ in ev_b]
+    diff = (out.float() - out_b.float()).abs()
+    bf16p = {"call": "grok_attn_prefill (no workspace; P as bf16 hi + lo)", "ms": float(np.mean(bf16p_times)),
+             "stats": time_stats(bf16p_times), "TFLOP/s": flops / (float(np.mean(bf16p_times)) * 1e-3) / 1e12,
+             "max_abs_diff_to_fp16_path": float(diff.max()), "mean_abs_diff_to_fp16_path": float(diff.mean())}
+    del out_b, diff
     ms, ms_prefill, ms_append = max_over_ranks([ms, ms_prefill, ms_append], dist, dev)
     value = whole_job_rate(flops, world, ms, 1e12)
     prefill_tflops = flops / (ms_prefill * 1e-3) / 1e12
@@ -349,13 +400,20 @@ def run_ours(args, rank: int, world: int, dist):
                    "parallelism": f"replicas x{world} (independent sequences, no exchange)"},
         "kernels_ms": {"rope_kv_append": ms_append, "prefill": ms_prefill},
         "kernels_ms_stats": {"rope_kv_append": time_stats(append_times), "prefill": time_stats(prefill_times)},
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": prefill_tflops, "peak": peak_tf,
+        "roofline": {"bound": "tensor",
+                     "kernel": "prefill_kernel<fp16> (timed over the whole grok_attn_prefill_ws call: V pre-pass, "
+                               "fp16 pass and the fallback pass)",
+                     "achieved": prefill_tflops, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": prefill_tflops / peak_tf, "peak_source": f"bf16_tflops ({peak_kind})",
+                     "frac_of_sustained": prefill_tflops / float(peaks.get("bf16_tflops_sustained",
+                                                                          FALLBACK_PEAKS["bf16_tflops_sustained"])),
                      "traffic": measured_traffic("prefill_kernel"), "traffic_unit": "bytes per launch (ncu)"},
+        "prefill_bf16_weights": bf16p,
         "append": {"GB/s": append_bytes(B, T) / (ms_append * 1e-3) / 1e9,
                    "frac_of_hbm": append_bytes(B, T) / (ms_append * 1e-3) / 1e9 / peak_bw},
         "clocks": clk,
-        "gpu_launches": 2 * args.steps,
+        # per step: append, V pre-pass, fp16 pass, fallback pass (the flag/list reset is a memset)
+        "gpu_launches": 4 * args.steps,
     }
 
     # ---------------- end to end through the public API with host buffers
@@ -376,7 +434,7 @@ def run_ours(args, rank: int, world: int, dist):
             v.copy_(vh, non_blocking=True)
             start.copy_(sh, non_blocking=True)
             G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
-            G.prefill(q_rot, ck, cv, start, valid, out, status)
+            G.prefill_ws(q_rot, ck, cv, start, valid, out, pf_ws, status)
             ohs[0].copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -418,8 +476,11 @@ def run_ours(args, rank: int, world: int, dist):
                          "ms_per_step_serial": ms_serial,
                          "value_serial": whole_job_rate(flops, world, ms_serial, 1e12)}
         del qh, kh, vh, ohs
-    del q, k, v, ck, cv, q_rot, out
+    del q, k, v, ck, cv, q_rot, out, pf_ws
     torch.cuda.empty_cache()
+
+    # ---------------- the other prefill workloads: ragged batch and chunk on a warm cache
+    result["other_prefill"] = run_other_prefill(args, rank, world, dist, dev, peaks, peak_kind)
 
     # ---------------- Q/K/V projection (the step in front of the attention call)
     if not args.no_qkv:
@@ -433,6 +494,67 @@ def run_ours(args, rank: int, world: int, dist):
     if not args.no_paged:
         result["paged"] = run_paged(args, rank, dev)
     return result
+
+
+def run_other_prefill(args, rank, world, dist, dev, peaks, peak_kind):
+    """Append + prefill on the ragged batch (B8, T2048, valid lengths U[256, 2048]) and the
+    chunk on a warm cache (B4, 256 tokens at 6144): CUDA events around each call."""
+    import torch
+
+    import grok_gqa_attention_gb300 as G
+    import workloads as W
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("ragged_prefill_b8_t2048", "chunked_prefill_b4_t256_at6144"):
+        inp = W.generate(name, seed=rank)
+        w = inp.workload
+        q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+        ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+        start = inp.start_pos.to(dev)
+        valid = None if inp.valid_len is None else inp.valid_len.to(dev)
+        valid_np = None if inp.valid_len is None else inp.valid_len.numpy()
+        q_rot, out = torch.empty_like(q), torch.empty_like(q)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = G.alloc_prefill_workspace(w.B, w.Tmax, dev)
+        flops = prefill_flops(inp.start_pos.numpy(), valid_np, w.T)
+        calls = {"append": lambda: G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status),
+                 "prefill_ws": lambda: G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status),
+                 "prefill_bf16_weights": lambda: G.prefill(q_rot, ck, cv, start, valid, out, status)}
+        times = {}
+        for key, fn in calls.items():
+            for _ in range(args.warmup):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+            for e in evs:
+                e[0].record(stream)
+                fn()
+                e[1].record(stream)
+            torch.cuda.synchronize()
+            times[key] = [a.elapsed_time(b_) for a, b_ in evs]
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in {name}")
+        ms = {key: max_over_ranks([float(np.mean(t))], dist, dev)[0] for key, t in times.items()}
+        entry = {"shape": {"B": w.B, "T": w.T, "Tmax": w.Tmax}, "algorithmic_gflop": flops / 1e9,
+                 "ms": ms, "stats": {key: time_stats(t) for key, t in times.items()},
+                 "prefill_TFLOP/s": flops / (ms["prefill_ws"] * 1e-3) / 1e12,
+                 "roofline": {"bound": "tensor", "frac": flops / (ms["prefill_ws"] * 1e-3) / 1e12 / peak_tf,
+                              "peak": peak_tf, "peak_source": f"bf16_tflops ({peak_kind})"},
+                 "prefill_bf16_weights_TFLOP/s": flops / (ms["prefill_bf16_weights"] * 1e-3) / 1e12,
+                 "step_TFLOP/s": whole_job_rate(flops, world, ms["append"] + ms["prefill_ws"], 1e12)}
+        if valid_np is not None:
+            # the padding query rows (i >= valid) are computed because the pages define them; without them:
+            s0 = inp.start_pos.numpy()
+            vis = sum(int((np.minimum(s0[b] + np.arange(int(n)), s0[b] + int(n) - 1) + 1).sum())
+                      for b, n in enumerate(valid_np))
+            entry["algorithmic_gflop_valid_rows_only"] = 48.0 * 4 * 128 * vis / 1e9
+        if name.startswith("chunked"):
+            entry["note"] = ("the call converts every cached V row [0, start + T) to fp16 each time "
+                             "(6400 rows per sequence here), part of the measured prefill time")
+        res[name] = entry
+        del q, k, v, ck, cv, q_rot, out, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 def _to_pool(cache, table, n_pages):
@@ -586,28 +708,41 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
     ms_i8, _ = timed(lambda: G.linear_int8(x2d, w8, scales, y, w16))
     deq_bytes = G.MODEL_SIZE * G.QKV_COLUMNS * 3 + G.QKV_COLUMNS * 4
     # decode-sized M (32 tokens): the one-pass int8 path against dequantize + bf16 product.
-    # The 50 MB int8 weight fits in L2, so a 256 MB buffer is written before each timed call.
+    # The 50 MB int8 weight fits in L2, so calls rotate over 5 distinct weights (250 MB,
+    # as a decode step walks the layers), and 10 calls are replayed from a CUDA graph so
+    # the device time is not hidden behind host launch overhead (a memset flush would
+    # leave ~130 MB of dirty lines whose write-back the next call would pay for).
     xs, ys = x2d[:32], y[:32]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    w8r = [w8] + [torch.randint(-127, 128, w8.shape, generator=gen, dtype=torch.int32).to(torch.int8).to(dev)
+                  for _ in range(4)]
 
-    def timed_cold(fn):
-        for _ in range(args.warmup):
-            fn()
+    def timed_graph(fn_i):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for i in range(len(w8r)):
+                fn_i(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(10):
+                fn_i(i)
         ts = []
-        for _ in range(max(5, min(args.steps, 20))):
-            flush.zero_()
+        for _ in range(max(3, min(args.steps, 10))):
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            fn()
+            g.replay()
             b_.record(stream)
             torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b_))
+            ts.append(a.elapsed_time(b_) / 10)
+        del g
         (m,) = max_over_ranks([float(np.median(ts))], dist, dev)
         return m
 
-    ms_i8s = timed_cold(lambda: G.linear_int8(xs, w8, scales, ys, w16))
-    ms_i8g = timed_cold(lambda: (G.dequant_int8(w8, scales, w16), G.linear(xs, w16, ys)))
-    del flush
+    ms_i8s = timed_graph(lambda i: G.linear_int8(xs, w8r[i % len(w8r)], scales, ys, w16, stream=torch.cuda.current_stream()))
+    ms_i8g = timed_graph(lambda i: (G.dequant_int8(w8r[i % len(w8r)], scales, w16, stream=torch.cuda.current_stream()),
+                                    G.linear(xs, w16, ys, stream=torch.cuda.current_stream())))
+    del w8r
     w8_bytes = G.MODEL_SIZE * G.QKV_COLUMNS
     torch.cuda.synchronize()
     if int(status.item()) != 0:
@@ -633,7 +768,8 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
                         "dequant_ms": ms_deq, "dequant_GB/s": deq_bytes / (ms_deq * 1e-3) / 1e9,
                         "dequant_frac_of_hbm": deq_bytes / (ms_deq * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                         "decode_sized": {"M": 32, "call": "grok_linear_int8 (one pass over the int8 weight)",
-                                         "timing": "median of calls each after a 256 MB write (L2 cold)",
+                                         "timing": "10 calls over 5 rotating 50 MB weights replayed from a CUDA graph "
+                                                   "(inputs larger than L2), median over replays",
                                          "ms": ms_i8s, "weight_GB/s": w8_bytes / (ms_i8s * 1e-3) / 1e9,
                                          "weight_frac_of_hbm": w8_bytes / (ms_i8s * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                                          "ms_dequant_then_linear": ms_i8g}},

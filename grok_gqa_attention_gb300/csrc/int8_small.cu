@@ -8,29 +8,33 @@
 // per element, 50 MB for the Q/K/V shape); x is tiny and stays in L2.
 //
 // Grid: (8, N / 256) in clusters of 8 CTAs along K. CTA (r, nb) owns output
-// columns [256 nb, 256 nb + 256) and weight rows [r K/8, (r+1) K/8). Each
-// weight row slice is 256 contiguous bytes, and 2 CTAs fit per SM, so the
-// whole grid of the Q/K/V shape (256 CTAs) is resident at once and every CTA
-// streams its own 196 KB.
+// columns [256 nb, 256 nb + 256) and weight rows [r K/8, (r+1) K/8); each
+// weight row slice is 256 contiguous bytes. Two CTAs fit per SM, so the whole
+// grid of the Q/K/V shape (256 CTAs) is resident at once.
 //
-// Per CTA (8 warps): a 3-stage ring of 64-row stages loaded by TMA, each
-// holding the stage's weight tile [64 rows x 256 bytes] and x tile
-// [16 MT rows x 64 bf16] (rows >= M are zero-filled by TMA; 128-byte swizzle).
-// Per stage:
-//   1. every warp loads the stage's A fragments of x (ldmatrix) into registers;
-//   2. all 256 threads dequantize the weight tile into a bf16 tile in shared
-//      memory, each element exactly as grok_dequant_int8 does it: the byte is
-//      turned into a float by placing it in the mantissa of 2^23 (byte permute)
-//      and subtracting 2^23 + 128, multiplied by its column scale with one
-//      fp32 rounding, then rounded to nearest-even bf16;
-//   3. a CTA barrier; the stage is free and thread 0 refills it with TMA;
-//   4. warp w multiplies the tile's columns [32 w, 32 w + 32) (mma.sync
-//      m16n8k16, B fragments by ldmatrix.trans), accumulating in fp32;
-//   5. a CTA barrier before the next stage overwrites the bf16 tile.
-// The 8 CTAs of a cluster then add their partial sums through distributed
-// shared memory in a fixed rank order (so results do not depend on
-// scheduling): CTA r sums columns [32 r, 32 r + 32) of all 8 partials, rounds
-// to bf16 and writes them.
+// Per CTA, three roles that run concurrently:
+//   warp 9     TMA producers: lane 0 streams the weight through a 3-stage
+//              ring of 64-row tiles [64 rows x 256 bytes], lane 1 the matching
+//              x tiles [16 MT rows x 64 bf16] (rows >= M zero-filled; 128-byte
+//              swizzle) through a 4-stage ring. Weight stages are released as
+//              soon as the converters hold their bytes in registers, x stages
+//              when the products that read them complete, so the weight stream
+//              never waits for the tensor core.
+//   warps 0-7  dequantize: each thread copies its 8 x 8 weight bytes of a stage
+//              to registers and releases the stage, then converts them into a
+//              2-stage ring of bf16 tiles [32 k x 256 n], stored as the
+//              MN-major, 128-byte-swizzled A operand (four 64-column blocks).
+//              Each element exactly as grok_dequant_int8 does it: the byte is
+//              turned into a float by placing it in the mantissa of 2^23 (byte
+//              permute) and subtracting 2^23 + 128, multiplied by its column
+//              scale with one fp32 rounding, then rounded to nearest-even bf16.
+//   warp 8     tcgen05.mma issuer (one lane) and TMEM owner: D[n, m] +=
+//              W^T[n, k] x^T[k, m] per 128-column half, M = 128 (n), N = 16 MT
+//              (m), K = 16, fp32 accumulators in TMEM (64 columns).
+// Then warps 0-7 read D (warp w: columns half w / 4, TMEM lanes 32 (w % 4)),
+// the 8 CTAs of a cluster add their partial sums through distributed shared
+// memory in a fixed rank order (so results do not depend on scheduling), and
+// CTA r rounds columns [32 r, 32 r + 32) to bf16 and writes them.
 #include "common.cuh"
 #include "host.cuh"
 
@@ -38,20 +42,36 @@ namespace grok {
 
 constexpr int kI8Cluster = 8;                      // CTAs along K
 constexpr int kI8Cols = 256;                       // output columns per CTA
-constexpr int kI8Rows = 64;                        // weight rows per stage
-constexpr int kI8Stages = 3;
-constexpr int kI8Threads = 256;
-constexpr int kI8XBytes = 32 * kI8Rows * 2;        // x tile (room for 32 rows)
+constexpr int kI8Rows = 64;                        // weight rows per TMA stage
+constexpr int kI8Stages = 3;                       // weight ring
+constexpr int kI8XStages = 4;                      // x ring
+constexpr int kI8ARows = 32;                       // k rows per bf16 A tile
+constexpr int kI8AStages = 2;
+constexpr int kI8DqWarps = 8;
+constexpr int kI8Threads = (kI8DqWarps + 2) * 32;  // + MMA warp + producer warp
+constexpr int kI8XBytes = 32 * kI8Rows * 2;        // x tile (room for 32 rows), 1024-byte aligned
 constexpr int kI8WBytes = kI8Rows * kI8Cols;       // int8 weight tile, 16 KB
-constexpr int kI8StageBytes = kI8XBytes + kI8WBytes;
-constexpr int kI8TileRow = kI8Cols * 2 + 16;       // bf16 tile row: 512 bytes + 16 of padding
-constexpr int kI8Tile = kI8Rows * kI8TileRow;
-constexpr int kI8Smem = kI8Stages * kI8StageBytes + kI8Tile + 64 + 1024;
-static_assert(32 * kI8Cols * 4 <= kI8Stages * kI8StageBytes, "partial sums must fit in the ring");
+constexpr int kI8ABlock = kI8ARows * 128;          // [32 k][64 n] bf16, 128-byte swizzled
+constexpr int kI8ABytes = 4 * kI8ABlock;           // 256 columns
+constexpr int kI8XOff = kI8Stages * kI8WBytes;     // x ring after the weight ring
+constexpr int kI8AOff = kI8XOff + kI8XStages * kI8XBytes;
+constexpr int kI8Data = kI8AOff + kI8AStages * kI8ABytes;
+constexpr int kI8Smem = kI8Data + 256 + 1024;
+static_assert(32 * kI8Cols * 4 <= kI8AStages * kI8ABytes, "partial sums must fit in the A ring");
 
-// 2-d tile load; the map must have been encoded with rank 2 (the instruction's
-// dimensionality must equal the map's rank).
+struct I8Bars {
+  uint64_t w_full[kI8Stages], w_empty[kI8Stages];
+  uint64_t x_full[kI8XStages], x_empty[kI8XStages];
+  uint64_t a_full[kI8AStages], a_empty[kI8AStages];
+  uint64_t d_full, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(I8Bars) <= 256, "barrier block");
+static_assert(kI8XOff % 1024 == 0 && kI8AOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  // the map must have been encoded with rank 2 (the instruction's dimensionality equals the map's rank)
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
@@ -100,145 +120,202 @@ __global__ void __cluster_dims__(kI8Cluster, 1, 1) __launch_bounds__(kI8Threads,
                              int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* tile = smem + kI8Stages * kI8StageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(tile + kI8Tile);
-  int* abort_flag = reinterpret_cast<int*>(full + kI8Stages);
-  volatile int* abort = abort_flag;
+  uint8_t* sA = smem + kI8AOff;
+  I8Bars* bars = reinterpret_cast<I8Bars*>(smem + kI8Data);
+  volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = blockIdx.x;  // position in the cluster = K slice
   const int n0 = blockIdx.y * kI8Cols;
-  const int rows = K / kI8Cluster;
-  const int k_first = rank * rows;
-  const int n_st = rows / kI8Rows;
-  constexpr uint32_t kStageTx = uint32_t(16 * MT * kI8Rows * 2 + kI8WBytes);
+  const int k_first = rank * (K / kI8Cluster);
+  const int n_st = K / kI8Cluster / kI8Rows;
+  constexpr uint32_t kXTx = uint32_t(16 * MT * kI8Rows * 2);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kI8Stages; ++s) mbar_init(&full[s], 1);
-    *abort_flag = 0;
+    for (int s = 0; s < kI8Stages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], kI8DqWarps * 32);  // every converter thread holds its bytes
+    }
+    for (int s = 0; s < kI8XStages; ++s) {
+      mbar_init(&bars->x_full[s], 1);
+      mbar_init(&bars->x_empty[s], 1);  // the products that read the tile completed
+    }
+    for (int s = 0; s < kI8AStages; ++s) {
+      mbar_init(&bars->a_full[s], kI8DqWarps * 32);
+      mbar_init(&bars->a_empty[s], 1);
+    }
+    mbar_init(&bars->d_full, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
     fence_barrier_init();
-    prefetch_tmap(&tm_x);
-    prefetch_tmap(&tm_w);
   }
+  if (warp == kI8DqWarps) {
+    tmem_alloc(&bars->tmem_base, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  auto load_stage = [&](int it) {
-    uint8_t* base = smem + (it % kI8Stages) * kI8StageBytes;
-    const int k = k_first + it * kI8Rows;
-    mbar_arrive_expect_tx(&full[it % kI8Stages], kStageTx);
-    tma_load_4d(base, &tm_x, &full[it % kI8Stages], k, 0, 0, 0);  // x's map is 4-d (rows, 1, 1)
-    tma_load_2d(base + kI8XBytes, &tm_w, &full[it % kI8Stages], n0, k);
-  };
-  if (threadIdx.x == 0)
-    for (int it = 0; it < kI8Stages && it < n_st; ++it) load_stage(it);
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
 
-  // this lane's 8 dequant columns 8 lane .. 8 lane + 7 and their scales
-  float sc[8];
-  {
-    const float4* s4 = reinterpret_cast<const float4*>(scales + n0 + 8 * lane);
-    const float4 a = __ldg(s4), b = __ldg(s4 + 1);
-    sc[0] = a.x, sc[1] = a.y, sc[2] = a.z, sc[3] = a.w, sc[4] = b.x, sc[5] = b.y, sc[6] = b.z, sc[7] = b.w;
-  }
-  float acc[MT][4][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-  const int mi = lane >> 3, mr = lane & 7;
-  const uint32_t tile_s = smem_u32(tile);
-  int issued = min(kI8Stages, n_st);  // stages whose copies were started (thread 0's count)
-  int consumed = 0;                    // stages whose copies landed (every thread's count)
-
-  for (int it = 0; it < n_st; ++it) {
-    const int st = it % kI8Stages;
-    const bool ok = __syncthreads_and(mbar_wait(&full[st], (it / kI8Stages) & 1, abort, status));
-    if (!ok) break;
-    ++consumed;
-    const uint8_t* xs = smem + st * kI8StageBytes;
-    const uint8_t* ws = xs + kI8XBytes;
-    // 1. A fragments of x: k steps kk of 16, rows mt*16 + (0..15)
-    uint32_t a[4][MT][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-        ldsm_x4(smem_u32(xs) + sw128_offset(mt * 16 + (mi & 1) * 8 + mr, kk * 16 + (mi >> 1) * 8), a[kk][mt][0],
-                a[kk][mt][1], a[kk][mt][2], a[kk][mt][3]);
-    // 2. dequantize: warp w rows 8w .. 8w+7, lane columns 8 lane .. +7
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const int row = warp * 8 + rr;
-      const uint2 raw = *reinterpret_cast<const uint2*>(ws + row * kI8Cols + 8 * lane);
-      float f[2][4];
-      i8x4_to_f32(raw.x, f[0]);
-      i8x4_to_f32(raw.y, f[1]);
-      uint32_t pk[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float p0, p1;
-        f2_unpack(f2_mul(f2_pack(f[q >> 1][2 * (q & 1)], f[q >> 1][2 * (q & 1) + 1]),
-                         f2_pack(sc[2 * q], sc[2 * q + 1])),
-                  p0, p1);
-        pk[q] = pack_bf16x2(p0, p1);
+  if (warp == kI8DqWarps + 1) {
+    // ------------------------------------------------------------ TMA producers
+    if (lane == 0) {  // weight tiles
+      prefetch_tmap(&tm_w);
+      int it = 0;
+      for (; it < n_st; ++it) {
+        const int st = it % kI8Stages;
+        if (!mbar_wait(&bars->w_empty[st], ((it / kI8Stages) & 1) ^ 1, abort, status)) break;
+        mbar_arrive_expect_tx(&bars->w_full[st], kI8WBytes);
+        tma_load_2d(smem + st * kI8WBytes, &tm_w, &bars->w_full[st], n0, k_first + it * kI8Rows);
       }
-      *reinterpret_cast<uint4*>(tile + row * kI8TileRow + 16 * lane) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      // copies still in flight (only after a wait gave up) land before the CTA exits
+      volatile int never = 0;
+      for (int t = max(0, it - kI8Stages); t < it; ++t)
+        mbar_wait(&bars->w_full[t % kI8Stages], (t / kI8Stages) & 1, &never, status);
+    } else if (lane == 1) {  // x tiles
+      prefetch_tmap(&tm_x);
+      int it = 0;
+      for (; it < n_st; ++it) {
+        const int st = it % kI8XStages;
+        if (!mbar_wait(&bars->x_empty[st], ((it / kI8XStages) & 1) ^ 1, abort, status)) break;
+        mbar_arrive_expect_tx(&bars->x_full[st], kXTx);
+        tma_load_4d(smem + kI8XOff + st * kI8XBytes, &tm_x, &bars->x_full[st], k_first + it * kI8Rows, 0, 0,
+                    0);  // x's map is 4-d (rows, 1, 1)
+      }
+      volatile int never = 0;
+      for (int t = max(0, it - kI8XStages); t < it; ++t)
+        mbar_wait(&bars->x_full[t % kI8XStages], (t / kI8XStages) & 1, &never, status);
     }
-    __syncthreads();
-    // 3. the stage is consumed: refill it
-    if (threadIdx.x == 0 && it + kI8Stages < n_st) {
-      load_stage(it + kI8Stages);
-      ++issued;
-    }
-    // 4. products for this warp's 32 columns
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int row = kk * 16 + (mi & 1) * 8 + mr, col = warp * 32 + np * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tile_s + row * kI8TileRow + col * 2, b0, b1, b2, b3);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16_16816(acc[mt][2 * np], a[kk][mt], b0, b1);
-          mma_bf16_16816(acc[mt][2 * np + 1], a[kk][mt], b2, b3);
+  } else if (warp == kI8DqWarps) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    // A: MN-major (n contiguous), 64-column blocks kI8ABlock apart, 8-row groups 1024 apart
+    const uint64_t ad = make_sdesc_sw128(smem_u32(sA), kI8ABlock, 1024);
+    // B = x^T: K-major (rows of x), 8-row groups 1024 apart
+    const uint64_t xd = make_sdesc_sw128(smem_u32(smem), 16, 1024);
+    constexpr uint32_t idesc = make_idesc_bf16(128, 16 * MT, 0) | (1u << 15);  // A MN-major
+    bool ok = true;
+    for (int it = 0; ok && it < n_st; ++it) {
+      const int st = it % kI8XStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->x_full[st], (it / kI8XStages) & 1, abort, status))) break;
+      for (int hs = 0; hs < kI8Rows / kI8ARows; ++hs) {
+        const int q = it * (kI8Rows / kI8ARows) + hs, a = q % kI8AStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->a_full[a], (q / kI8AStages) & 1, abort, status))) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+            for (int kk = 0; kk < kI8ARows / 16; ++kk) {
+              const uint64_t adesc = ad + uint64_t((a * kI8ABytes + nh * 2 * kI8ABlock + kk * 2048) >> 4);
+              const uint64_t bdesc =
+                  xd + uint64_t((kI8XOff + st * kI8XBytes + (hs * (kI8ARows / 16) + kk) * 32) >> 4);
+              umma_ss(tmem + nh * 32, adesc, bdesc, idesc, (it > 0 || hs > 0 || kk > 0) ? 1u : 0u);
+            }
+          umma_commit(&bars->a_empty[a]);
+          if (hs == kI8Rows / kI8ARows - 1) umma_commit(&bars->x_empty[st]);  // the x tile is read
+        }
+        __syncwarp();
       }
     }
-    __syncthreads();  // 5. the tile is read before the next stage's dequant
-  }
-  // Copies still in flight (only after a wait gave up) land before the ring is reused.
-  if (threadIdx.x == 0) {
+    if (leader) {
+      umma_commit(&bars->d_full);
+      umma_commit(&bars->mma_done);
+    }
+    __syncwarp();
     volatile int never = 0;
-    for (int t = consumed; t < issued; ++t) mbar_wait(&full[t % kI8Stages], (t / kI8Stages) & 1, &never, status);
-  }
-  __syncthreads();
-  // Partial sums into the ring: part[row][col], rows 0 .. 16 MT - 1, 256 columns.
-  float* part = reinterpret_cast<float*>(smem);
-  {
-    const int g = lane >> 2, t = lane & 3;
+    mbar_wait(&bars->mma_done, 0, &never, status);
+  } else {
+    // ------------------------------------------------------------ converters
+    float sc[8];  // this lane's columns 8 lane .. 8 lane + 7
+    {
+      const float4* s4 = reinterpret_cast<const float4*>(scales + n0 + 8 * lane);
+      const float4 u = __ldg(s4), v = __ldg(s4 + 1);
+      sc[0] = u.x, sc[1] = u.y, sc[2] = u.z, sc[3] = u.w, sc[4] = v.x, sc[5] = v.y, sc[6] = v.z, sc[7] = v.w;
+    }
+    // where this lane's 8 columns go in an A tile row: 64-column block lane / 8, 16-byte chunk lane % 8
+    const int blk = lane >> 3, chunk = lane & 7;
+    bool ok = true;
+    for (int it = 0; ok && it < n_st; ++it) {
+      const int st = it % kI8Stages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->w_full[st], (it / kI8Stages) & 1, abort, status))) break;
+      // rows warp + 8 i of the stage, i = 0..7
+      const uint8_t* ws = smem + st * kI8WBytes;
+      uint2 raw[8];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int i = 0; i < 8; ++i) raw[i] = *reinterpret_cast<const uint2*>(ws + (warp + 8 * i) * kI8Cols + 8 * lane);
+      mbar_arrive(&bars->w_empty[st]);
+      for (int hs = 0; hs < kI8Rows / kI8ARows; ++hs) {
+        const int q = it * (kI8Rows / kI8ARows) + hs, a = q % kI8AStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->a_empty[a], ((q / kI8AStages) & 1) ^ 1, abort, status))) {
+          ok = false;
+          break;
+        }
+        uint8_t* at = sA + a * kI8ABytes + blk * kI8ABlock;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+        for (int i = 0; i < 4; ++i) {
+          const int row = warp + 8 * i;  // k row within the A tile (rows of raw[4 hs + i])
+          const uint2 r2 = raw[4 * hs + i];
+          float f[2][4];
+          i8x4_to_f32(r2.x, f[0]);
+          i8x4_to_f32(r2.y, f[1]);
+          uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          part[(mt * 16 + g + 8 * (e >> 1)) * kI8Cols + warp * 32 + nt * 8 + 2 * t + (e & 1)] = acc[mt][nt][e];
-  }
-  cluster_sync();  // every CTA's partial sums are in its shared memory
-  // CTA `rank` finishes columns [32 rank, 32 rank + 32): pairs of columns, rows < M
-  for (int o = threadIdx.x; o < 16 * MT * 16; o += kI8Threads) {
-    const int row = o / 16, col = 32 * rank + 2 * (o % 16);
-    if (row < M) {
-      const uint32_t local = smem_u32(part + row * kI8Cols + col);
-      float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-      for (int q = 0; q < kI8Cluster; ++q) {  // fixed order
-        const float2 v = ld_dsmem_f2(dsmem_addr(local, uint32_t(q)));
-        v0 += v.x;
-        v1 += v.y;
+          for (int e = 0; e < 4; ++e) {
+            float p0, p1;
+            f2_unpack(f2_mul(f2_pack(f[e >> 1][2 * (e & 1)], f[e >> 1][2 * (e & 1) + 1]),
+                             f2_pack(sc[2 * e], sc[2 * e + 1])),
+                      p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(at + row * 128 + ((chunk ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();  // the generic-proxy stores become visible to the tensor core
+        mbar_arrive(&bars->a_full[a]);
       }
-      y[(size_t(row) * N + n0 + col) / 2] = pack_bf16x2(v0, v1);
+    }
+    // D -> partial sums part[m][n] in the A ring (all products are complete)
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars->d_full, 0, abort, status));
+    tc_fence_after();
+    float* part = reinterpret_cast<float*>(sA);
+    const int nh = warp >> 2, quad = warp & 3;
+    uint32_t d[32];
+    tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + nh * 32, d);
+    tmem_wait_ld_dep(d);
+    if (done) {
+      const int n = nh * 128 + quad * 32 + lane;
+#pragma unroll
+      for (int m = 0; m < 16 * MT; ++m) part[m * kI8Cols + n] = __uint_as_float(d[m]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // every CTA's partial sums are in its shared memory
+  if (warp < kI8DqWarps) {
+    float* part = reinterpret_cast<float*>(sA);
+    // CTA `rank` finishes columns [32 rank, 32 rank + 32): pairs of columns, rows < M
+    for (int o = threadIdx.x; o < 16 * MT * 16; o += kI8DqWarps * 32) {
+      const int row = o / 16, col = 32 * rank + 2 * (o % 16);
+      if (row < M) {
+        const uint32_t local = smem_u32(part + row * kI8Cols + col);
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kI8Cluster; ++q) {  // fixed order
+          const float2 v = ld_dsmem_f2(dsmem_addr(local, uint32_t(q)));
+          v0 += v.x;
+          v1 += v.y;
+        }
+        y[(size_t(row) * N + n0 + col) / 2] = pack_bf16x2(v0, v1);
+      }
     }
   }
   cluster_sync();  // no CTA leaves while another reads its shared memory
+  if (warp == kI8DqWarps) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
 }
 
 bool small_int8_ok(int M, int K, int N) {

@@ -1,6 +1,6 @@
-// Host-buffer prefill pipeline: grok_rope_kv_append + grok_attn_prefill fed
-// from host memory, with the copies of one step overlapping the kernels of the
-// steps around it.
+// Host-buffer prefill pipeline: grok_rope_kv_append + grok_attn_prefill_ws (the
+// prefill with fp16 softmax weights) fed from host memory, with the copies of
+// one step overlapping the kernels of the steps around it.
 //
 // Three streams: host-to-device copies, kernels, device-to-host copies. Inputs
 // and outputs are double-buffered on the device (two slots, used alternately);
@@ -24,6 +24,8 @@ struct grok_prefill_pipe {
     bool used = false;
   } slot[2];
   grok_bf16* q_rot = nullptr;
+  void* pf_ws = nullptr;      // grok_attn_prefill_ws workspace (used in kernel-stream order)
+  size_t pf_ws_bytes = 0;
   int32_t* status = nullptr;  // OR of every step's device status since the last wait
   long long submitted = 0;
 };
@@ -61,6 +63,7 @@ void release(grok_prefill_pipe* p) {
     if (s.out_done) cudaEventDestroy(s.out_done);
   }
   cudaFree(p->q_rot);
+  cudaFree(p->pf_ws);
   cudaFree(p->status);
   if (p->s_in) cudaStreamDestroy(p->s_in);
   if (p->s_run) cudaStreamDestroy(p->s_run);
@@ -110,6 +113,11 @@ extern "C" grok_status grok_prefill_pipe_create(int B, int T, int Tmax, grok_bf1
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.out_done, cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaMalloc(&p->q_rot, nq);
+  if (e == cudaSuccess && (st = grok_attn_prefill_workspace(B, Tmax, &p->pf_ws_bytes)) != GROK_OK) {
+    release(p);
+    return st;
+  }
+  if (e == cudaSuccess) e = cudaMalloc(&p->pf_ws, p->pf_ws_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking);
@@ -148,8 +156,8 @@ extern "C" grok_status grok_prefill_pipe_submit(grok_prefill_pipe* p, const grok
   grok_status st = grok_rope_kv_append(s.q, s.k, s.v, s.start, p->B, p->T, p->Tmax, p->q_rot, p->cache_k,
                                        p->cache_v, p->status, p->s_run);
   if (st != GROK_OK) return st;
-  st = grok_attn_prefill(p->q_rot, p->cache_k, p->cache_v, s.start, valid_len ? s.valid : nullptr, p->B, p->T,
-                         p->Tmax, s.out, p->status, p->s_run);
+  st = grok_attn_prefill_ws(p->q_rot, p->cache_k, p->cache_v, s.start, valid_len ? s.valid : nullptr, p->B, p->T,
+                            p->Tmax, s.out, p->pf_ws, p->pf_ws_bytes, p->status, p->s_run);
   if (st != GROK_OK) return st;
   e = cudaEventRecord(s.run_done, p->s_run);
   // copy-out

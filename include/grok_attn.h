@@ -373,10 +373,11 @@ grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const i
  *   [B,Tmax,8,128] bf16 (16-byte aligned): every step appends to them and
  *   attends over them, and they must stay allocated until destroy. Allocates
  *   about B*T*(5*48 + 4*8)*128*2 bytes of device memory on the current device,
- *   which the pipeline uses from then on. *pipe receives the handle.
+ *   plus grok_attn_prefill_workspace(B, Tmax) bytes, which the pipeline uses
+ *   from then on. *pipe receives the handle.
  * grok_prefill_pipe_submit: queue one step. Copy q [B,T,48,128], k and v
  *   [B,T,8,128], start_pos [B] and valid_len [B] (NULL: every token valid) from
- *   host memory; run grok_rope_kv_append then grok_attn_prefill; copy the output
+ *   host memory; run grok_rope_kv_append then grok_attn_prefill_ws; copy the output
  *   [B,T,48,128] to host memory at out. Returns once the work is queued. The
  *   host buffers must stay valid, the inputs unchanged and the output unread
  *   until the next grok_prefill_pipe_wait. Page-locked host memory

@@ -2,8 +2,8 @@
 
 Several chunked-prefill steps are queued back to back (their copies overlap
 each other's kernels); each step's output and the final caches must equal, bit
-for bit, those of grok_rope_kv_append + grok_attn_prefill called step by step
-on device tensors, which the other parity tests hold to the oracle.
+for bit, those of grok_rope_kv_append + grok_attn_prefill_ws called step by
+step on device tensors, which the other parity tests hold to the oracle.
 """
 import ctypes
 
@@ -48,7 +48,7 @@ def test_pipeline_matches_step_by_step_device_calls():
         q_rot = torch.empty_like(q)
         out = torch.empty_like(q)
         G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
-        G.prefill(q_rot, ck, cv, start, valid, out, status)
+        G.prefill_ws(q_rot, ck, cv, start, valid, out, G.alloc_prefill_workspace(B, TMAX), status)
         ref.append(W.bits(out.cpu()))
     torch.cuda.synchronize()
     assert int(status.item()) == 0
