@@ -315,6 +315,8 @@ def run_ours(args, rank: int, world: int, dist):
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     pf_ws = G.alloc_prefill_workspace(B, Tmax, dev)
+    # cos/sin of every position, computed once (a model shares it across all layers and steps)
+    cos_tab, sin_tab = G.rope_cos_sin(0, Tmax)
     flops = prefill_flops(inp.start_pos.numpy(), None if inp.valid_len is None else inp.valid_len.numpy(), T)
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -323,7 +325,7 @@ def run_ours(args, rank: int, world: int, dist):
     def step(e=None):
         if e is not None:
             e[0].record(stream)
-        G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+        G.rope_kv_append_table(q, k, v, start, cos_tab, sin_tab, q_rot, ck, cv, status)
         if e is not None:
             e[1].record(stream)
         G.prefill_ws(q_rot, ck, cv, start, valid, out, pf_ws, status)
@@ -371,6 +373,20 @@ def run_ours(args, rank: int, world: int, dist):
         e[1].record(stream)
     torch.cuda.synchronize()
     bf16p_times = [a.elapsed_time(b_) for a, b_ in ev_b]
+    # context: the append that evaluates its cos/sin per token instead of reading the table
+    q_rot_e = torch.empty_like(q_rot)
+    for _ in range(args.warmup):
+        G.rope_kv_append(q, k, v, start, q_rot_e, ck, cv, status)
+    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e in ev_e:
+        e[0].record(stream)
+        G.rope_kv_append(q, k, v, start, q_rot_e, ck, cv, status)
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    append_eval_times = [a.elapsed_time(b_) for a, b_ in ev_e]
+    if not torch.equal(q_rot_e.view(torch.int16), q_rot.view(torch.int16)):
+        raise RuntimeError("the table append and the evaluating append differ")
+    del q_rot_e
     diff = (out.float() - out_b.float()).abs()
     bf16p = {"call": "grok_attn_prefill (no workspace; P as bf16 hi + lo)", "ms": float(np.mean(bf16p_times)),
              "stats": time_stats(bf16p_times), "TFLOP/s": flops / (float(np.mean(bf16p_times)) * 1e-3) / 1e12,
@@ -409,10 +425,14 @@ def run_ours(args, rank: int, world: int, dist):
                                                                           FALLBACK_PEAKS["bf16_tflops_sustained"])),
                      "traffic": measured_traffic("prefill_kernel"), "traffic_unit": "bytes per launch (ncu)"},
         "prefill_bf16_weights": bf16p,
-        "append": {"GB/s": append_bytes(B, T) / (ms_append * 1e-3) / 1e9,
-                   "frac_of_hbm": append_bytes(B, T) / (ms_append * 1e-3) / 1e9 / peak_bw},
+        "append": {"call": "grok_rope_kv_append_table (cos/sin table of every position computed once "
+                           "before timing, shared by all layers and steps)",
+                   "GB/s": append_bytes(B, T) / (ms_append * 1e-3) / 1e9,
+                   "frac_of_hbm": append_bytes(B, T) / (ms_append * 1e-3) / 1e9 / peak_bw,
+                   "evaluating_cos_sin_per_token": {"call": "grok_rope_kv_append", "stats": time_stats(append_eval_times),
+                                                    "GB/s": append_bytes(B, T) / (float(np.mean(append_eval_times)) * 1e-3) / 1e9}},
         "clocks": clk,
-        # per step: append, V pre-pass, fp16 pass, fallback pass (the flag/list reset is a memset)
+        # per step: append (table), V pre-pass, fp16 pass, fallback pass (the flag/list reset is a memset)
         "gpu_launches": 4 * args.steps,
     }
 
@@ -433,7 +453,7 @@ def run_ours(args, rank: int, world: int, dist):
             k.copy_(kh, non_blocking=True)
             v.copy_(vh, non_blocking=True)
             start.copy_(sh, non_blocking=True)
-            G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+            G.rope_kv_append_table(q, k, v, start, cos_tab, sin_tab, q_rot, ck, cv, status)
             G.prefill_ws(q_rot, ck, cv, start, valid, out, pf_ws, status)
             ohs[0].copy_(out, non_blocking=True)
 
@@ -476,7 +496,7 @@ def run_ours(args, rank: int, world: int, dist):
                          "ms_per_step_serial": ms_serial,
                          "value_serial": whole_job_rate(flops, world, ms_serial, 1e12)}
         del qh, kh, vh, ohs
-    del q, k, v, ck, cv, q_rot, out, pf_ws
+    del q, k, v, ck, cv, q_rot, out, pf_ws, cos_tab, sin_tab
     torch.cuda.empty_cache()
 
     # ---------------- the other prefill workloads: ragged batch and chunk on a warm cache

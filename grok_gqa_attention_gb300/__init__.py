@@ -42,6 +42,7 @@ EXPORTS = (
     "grok_last_error",
     "grok_cuda_error_status",
     "grok_rope_kv_append",
+    "grok_rope_kv_append_table",
     "grok_rope_cos_sin",
     "grok_attn_prefill",
     "grok_attn_prefill_workspace",
@@ -97,6 +98,8 @@ def load() -> ctypes.CDLL:
     lib.grok_cuda_error_status.argtypes = [I]
     lib.grok_rope_kv_append.restype = I
     lib.grok_rope_kv_append.argtypes = [P, P, P, P, I, I, I, P, P, P, P, P]
+    lib.grok_rope_kv_append_table.restype = I
+    lib.grok_rope_kv_append_table.argtypes = [P, P, P, P, I, I, I, P, P, I, P, P, P, P, P]
     lib.grok_rope_cos_sin.restype = I
     lib.grok_rope_cos_sin.argtypes = [I, I, P, P, P]
     lib.grok_attn_prefill.restype = I
@@ -104,7 +107,7 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_prefill_workspace.restype = I
     lib.grok_attn_prefill_workspace.argtypes = [I, I, ctypes.POINTER(S)]
     lib.grok_attn_prefill_ws.restype = I
-    lib.grok_attn_prefill_ws.argtypes = [P, P, P, P, P, I, I, I, P, P, S, P, P]
+    lib.grok_attn_prefill_ws.argtypes = [P, P, P, P, P, I, I, I, P, P, S, I, P, P]
     lib.grok_attn_decode_workspace.restype = I
     lib.grok_attn_decode_workspace.argtypes = [I, I, ctypes.POINTER(S), ctypes.POINTER(I)]
     lib.grok_attn_decode.restype = I
@@ -204,6 +207,28 @@ def rope_kv_append(q, k, v, start_pos, q_rot, cache_k, cache_v, dev_status=None,
                                       _ptr(cache_k), _ptr(cache_v), _ptr(dev_status), _stream(stream)))
 
 
+def rope_kv_append_table(q, k, v, start_pos, cos_tab, sin_tab, q_rot, cache_k, cache_v, dev_status=None,
+                         stream=None) -> None:
+    """rope_kv_append with cos/sin read from a table of positions [0, n) (see rope_cos_sin(0, n))."""
+    B, T = q.shape[0], q.shape[1]
+    Tmax = cache_k.shape[1]
+    n = cos_tab.shape[0]
+    _want(q, "q", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(k, "k", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(v, "v", torch.bfloat16, (B, T, N_KV_HEADS, HEAD_DIM))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(cos_tab, "cos_tab", torch.float32, (n, 64))
+    _want(sin_tab, "sin_tab", torch.float32, (n, 64))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_rope_kv_append_table(_ptr(q), _ptr(k), _ptr(v), _ptr(start_pos), B, T, Tmax, _ptr(cos_tab),
+                                            _ptr(sin_tab), n, _ptr(q_rot), _ptr(cache_k), _ptr(cache_v),
+                                            _ptr(dev_status), _stream(stream)))
+
+
 def rope_cos_sin(first_position: int, n_positions: int, stream=None):
     """The fp32 cos/sin table [n_positions, 64] the append kernel uses (new CUDA tensors)."""
     c = torch.empty((n_positions, 64), dtype=torch.float32, device="cuda")
@@ -240,8 +265,12 @@ def alloc_prefill_workspace(B: int, Tmax: int, device=None) -> torch.Tensor:
     return torch.empty(prefill_workspace(B, Tmax), dtype=torch.uint8, device=device or "cuda")
 
 
-def prefill_ws(q_rot, cache_k, cache_v, start_pos, valid_len, out, workspace, dev_status=None, stream=None) -> None:
-    """prefill() with fp16 softmax weights and an fp16 copy of V in `workspace` (uint8 CUDA tensor)."""
+def prefill_ws(q_rot, cache_k, cache_v, start_pos, valid_len, out, workspace, dev_status=None, stream=None,
+               reuse_v_half: bool = False) -> None:
+    """prefill() with fp16 softmax weights and an fp16 copy of V in `workspace` (uint8 CUDA tensor).
+
+    reuse_v_half: rows below start_pos are already in the workspace from earlier calls
+    over the same caches (see grok_attn_prefill_ws)."""
     B, T = q_rot.shape[0], q_rot.shape[1]
     Tmax = cache_k.shape[1]
     _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
@@ -256,7 +285,7 @@ def prefill_ws(q_rot, cache_k, cache_v, start_pos, valid_len, out, workspace, de
         _want(dev_status, "dev_status", torch.int32, (1,))
     _check(load().grok_attn_prefill_ws(_ptr(q_rot), _ptr(cache_k), _ptr(cache_v), _ptr(start_pos),
                                        _ptr(valid_len), B, T, Tmax, _ptr(out), _ptr(workspace), workspace.numel(),
-                                       _ptr(dev_status), _stream(stream)))
+                                       1 if reuse_v_half else 0, _ptr(dev_status), _stream(stream)))
 
 
 def decode_workspace(B: int, Tmax: int) -> tuple[int, int]:

@@ -1,4 +1,5 @@
-// Host-buffer prefill pipeline: grok_rope_kv_append + grok_attn_prefill_ws (the
+// Host-buffer prefill pipeline: grok_rope_kv_append_table (with a cos/sin table
+// of positions [0, Tmax) computed once at create) + grok_attn_prefill_ws (the
 // prefill with fp16 softmax weights) fed from host memory, with the copies of
 // one step overlapping the kernels of the steps around it.
 //
@@ -25,6 +26,8 @@ struct grok_prefill_pipe {
   } slot[2];
   grok_bf16* q_rot = nullptr;
   void* pf_ws = nullptr;      // grok_attn_prefill_ws workspace (used in kernel-stream order)
+  float* cos_tab = nullptr;   // RoPE table of positions [0, Tmax)
+  float* sin_tab = nullptr;
   size_t pf_ws_bytes = 0;
   int32_t* status = nullptr;  // OR of every step's device status since the last wait
   long long submitted = 0;
@@ -64,6 +67,8 @@ void release(grok_prefill_pipe* p) {
   }
   cudaFree(p->q_rot);
   cudaFree(p->pf_ws);
+  cudaFree(p->cos_tab);
+  cudaFree(p->sin_tab);
   cudaFree(p->status);
   if (p->s_in) cudaStreamDestroy(p->s_in);
   if (p->s_run) cudaStreamDestroy(p->s_run);
@@ -118,6 +123,8 @@ extern "C" grok_status grok_prefill_pipe_create(int B, int T, int Tmax, grok_bf1
     return st;
   }
   if (e == cudaSuccess) e = cudaMalloc(&p->pf_ws, p->pf_ws_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&p->cos_tab, size_t(Tmax) * 64 * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&p->sin_tab, size_t(Tmax) * 64 * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking);
@@ -126,6 +133,10 @@ extern "C" grok_status grok_prefill_pipe_create(int B, int T, int Tmax, grok_bf1
   if (e != cudaSuccess) {
     release(p);
     return cuda_fail("create", e);
+  }
+  if ((st = grok_rope_cos_sin(0, Tmax, p->cos_tab, p->sin_tab, p->s_run)) != GROK_OK) {
+    release(p);
+    return st;
   }
   *pipe = p;
   return GROK_OK;
@@ -153,11 +164,11 @@ extern "C" grok_status grok_prefill_pipe_submit(grok_prefill_pipe* p, const grok
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p->s_run, s.in_done, 0);
   if (e == cudaSuccess && s.used) e = cudaStreamWaitEvent(p->s_run, s.out_done, 0);
   if (e != cudaSuccess) return cuda_fail("enqueue copy-in", e);
-  grok_status st = grok_rope_kv_append(s.q, s.k, s.v, s.start, p->B, p->T, p->Tmax, p->q_rot, p->cache_k,
-                                       p->cache_v, p->status, p->s_run);
+  grok_status st = grok_rope_kv_append_table(s.q, s.k, s.v, s.start, p->B, p->T, p->Tmax, p->cos_tab, p->sin_tab,
+                                             p->Tmax, p->q_rot, p->cache_k, p->cache_v, p->status, p->s_run);
   if (st != GROK_OK) return st;
   st = grok_attn_prefill_ws(p->q_rot, p->cache_k, p->cache_v, s.start, valid_len ? s.valid : nullptr, p->B, p->T,
-                            p->Tmax, s.out, p->pf_ws, p->pf_ws_bytes, p->status, p->s_run);
+                            p->Tmax, s.out, p->pf_ws, p->pf_ws_bytes, 0, p->status, p->s_run);
   if (st != GROK_OK) return st;
   e = cudaEventRecord(s.run_done, p->s_run);
   // copy-out

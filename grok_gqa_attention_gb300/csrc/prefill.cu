@@ -235,6 +235,8 @@ __device__ __forceinline__ void pf_issue_pv_half(uint32_t d, uint32_t pbase, uin
 
 // Column pairs of a 32-key chunk whose exp2 runs on the FMA pipe (bit e: pair
 // e); the rest use the special-function unit, which also evaluates every tanh.
+// Half is best in both modes (fp16 mode: 0.668 ms with half, 0.706 with three
+// quarters, 0.747 with all on prefill_b1_t8192).
 constexpr uint32_t kPolyPairs = 0x3333;
 
 // S -> P for one 32-key chunk c of one row (this thread's TMEM lane): weights
@@ -682,16 +684,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // reads is finite. A finite |v| >= 65520 (beyond fp16) sets v_flags[b]: the
 // fp16 pass then hands all of that sequence's items to the fallback pass.
 __global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict__ cache_v, const int32_t* start_pos,
-                                                        int T, int Tmax, int vh_rows, uint4* __restrict__ vh,
-                                                        int32_t* v_flags) {
+                                                        int T, int Tmax, int vh_rows, int from_start,
+                                                        uint4* __restrict__ vh, int32_t* v_flags) {
   const int b = blockIdx.y;
   const int s = __ldg(start_pos + b);
   if (s < 0 || (long long)s + T > Tmax) return;  // the attention passes skip this sequence
   const int rows = s + T, rows_pad = min(vh_rows, (rows + kPfKeys - 1) / kPfKeys * kPfKeys);
+  const int first = from_start ? s : 0;  // rows below `first` are already converted (reuse)
   constexpr int kChunks = kKVHeads * kD / 8;  // 16-byte chunks (8 values) per row
   bool over = false;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)rows_pad * kChunks;
-       e += (long long)gridDim.x * blockDim.x) {
+  for (long long e = (long long)first * kChunks + (long long)blockIdx.x * blockDim.x + threadIdx.x;
+       e < (long long)rows_pad * kChunks; e += (long long)gridDim.x * blockDim.x) {
     const int row = int(e / kChunks), ch = int(e % kChunks);
     uint4 out = make_uint4(0, 0, 0, 0);
     if (row < rows) {
@@ -866,8 +869,8 @@ extern "C" grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* byte
 extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k,
                                             const grok_bf16* cache_v, const int32_t* start_pos,
                                             const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
-                                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                            void* stream) {
+                                            void* workspace, size_t workspace_bytes, int reuse_v_half,
+                                            int32_t* dev_status, void* stream) {
   if (!q_rot || !cache_k || !cache_v || !start_pos || !out || !workspace)
     return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: null pointer");
   if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
@@ -892,16 +895,19 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
   void* vh = static_cast<char*>(workspace) + ws_header_bytes(B, Tmax);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  cudaError_t e = cudaMemsetAsync(v_flags, 0, (size_t(B) + 1) * sizeof(int32_t), s);  // flags and list count
+  // the list count, and unless the copy is reused the overflow flags (reused: they persist)
+  cudaError_t e = reuse_v_half ? cudaMemsetAsync(fb_count, 0, sizeof(int32_t), s)
+                               : cudaMemsetAsync(v_flags, 0, (size_t(B) + 1) * sizeof(int32_t), s);
   if (e != cudaSuccess) return fail(cuda_status(e), "cudaMemsetAsync: %s", cudaGetErrorString(e));
   {
-    const long long per_seq = (long long)vh_rows * (kKVHeads * kD / 8);
+    const long long per_seq = (long long)(reuse_v_half ? ((T + 2 * kPfKeys - 1) / kPfKeys * kPfKeys) : vh_rows) *
+                              (kKVHeads * kD / 8);
     long long bx = (per_seq + 255) / 256;
     const long long cap = ((long long)sms * 8 + B - 1) / B;  // about 8 blocks per SM in all
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
     v_to_half_kernel<<<dim3(unsigned(bx), unsigned(B)), 256, 0, s>>>(reinterpret_cast<const uint4*>(cache_v),
-                                                                     start_pos, T, Tmax, vh_rows,
+                                                                     start_pos, T, Tmax, vh_rows, reuse_v_half ? 1 : 0,
                                                                      static_cast<uint4*>(vh), v_flags);
     if ((st = check_launch("v_to_half")) != GROK_OK) return st;
   }

@@ -16,6 +16,13 @@
 // result is bit-for-bit the fp32 chain.
 //
 // Memory-bound: per token it reads 14 KB (q, k, v) and writes 14 KB.
+//
+// Table variant (kTab, grok_rope_kv_append_table): the (cos, sin) pairs are
+// read from a table of positions [0, n) that grok_rope_cos_sin filled once
+// (the values depend only on the position, so one table serves every layer
+// and step), instead of being evaluated per token: 512 bytes of L2-resident
+// table per token in place of 64 fp64 cos/sin evaluations. The table holds
+// the same fp32 values the evaluation gives, so the bits are the same.
 #include "common.cuh"
 #include "host.cuh"
 #include "rope_math.cuh"
@@ -57,11 +64,12 @@ __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const 
 // warps.
 constexpr int kRopeWarps = kRopeThreads / 32;
 
-template <int team>
+template <int team, bool kTab>
 __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const int32_t* __restrict__ start_pos, int B, int T, int Tmax, uint4* __restrict__ q_rot,
-    uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, PageMap pm, int32_t* status) {
+    uint4* __restrict__ cache_k, uint4* __restrict__ cache_v, PageMap pm, const float4* __restrict__ cos_tab,
+    const float4* __restrict__ sin_tab, int tab_n, int32_t* status) {
   // A kernel launched as this grid's programmatic dependent (the decode step's
   // split-K decode) may start at once; it waits for this grid before reading
   // what it writes.
@@ -70,8 +78,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
   __shared__ float s_cos[kRopeWarps][64];
   __shared__ float s_sin[kRopeWarps][64];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid < 64) s_inv[tid] = rope_inv_freq(tid);
-  __syncthreads();
+  if (!kTab) {
+    if (tid < 64) s_inv[tid] = rope_inv_freq(tid);
+    __syncthreads();
+  }
   const long long ntok = (long long)B * T;
   const long long gw = (long long)blockIdx.x * kRopeWarps + warp;
   const int member = int(gw % team);
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
     const int b = int(tok / T);
     const int i = int(tok - (long long)b * T);
     const int s0 = __ldg(start_pos + b);
-    const bool ok = s0 >= 0 && (long long)s0 + T <= Tmax && (long long)s0 + T <= GROK_MAX_POSITION;
+    const bool ok = s0 >= 0 && (long long)s0 + T <= Tmax && (long long)s0 + T <= (kTab ? tab_n : GROK_MAX_POSITION);
     if (!ok) {  // uniform over the warp
       if (lane == 0 && i == 0 && member == 0) report(status, GROK_DEV_BAD_START);
       continue;
@@ -114,17 +124,32 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_append_kernel(
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       if (m % team == member) vv[m] = __ldg(v + (size_t)tok * (kKVHeads * 16) + lane + 32 * m);
-    __syncwarp();  // the previous token's table is no longer read
-    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
-    rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
-    __syncwarp();
+    // Every unit of this lane rotates pairs 8c .. 8c+7 with c = lane % 8.
+    float tc[8], ts[8];
+    if (kTab) {
+      const size_t t0 = (size_t)pos * 16 + 2 * (lane & 7);  // float4 index of (pos, 8c)
+      const float4 c0 = __ldg(cos_tab + t0), c1 = __ldg(cos_tab + t0 + 1);
+      const float4 d0 = __ldg(sin_tab + t0), d1 = __ldg(sin_tab + t0 + 1);
+      tc[0] = c0.x, tc[1] = c0.y, tc[2] = c0.z, tc[3] = c0.w, tc[4] = c1.x, tc[5] = c1.y, tc[6] = c1.z, tc[7] = c1.w;
+      ts[0] = d0.x, ts[1] = d0.y, ts[2] = d0.z, ts[3] = d0.w, ts[4] = d1.x, ts[5] = d1.y, ts[6] = d1.z, ts[7] = d1.w;
+    } else {
+      __syncwarp();  // the previous token's table is no longer read
+      rope_cos_sin(__fmul_rn(float(pos), s_inv[lane]), s_cos[warp][lane], s_sin[warp][lane]);
+      rope_cos_sin(__fmul_rn(float(pos), s_inv[lane + 32]), s_cos[warp][lane + 32], s_sin[warp][lane + 32]);
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        tc[e] = s_cos[warp][8 * (lane & 7) + e];
+        ts[e] = s_sin[warp][8 * (lane & 7) + e];
+      }
+    }
 #pragma unroll
     for (int m = 0; m < 14; ++m) {
       if (m % team != member) continue;
       const int u = lane + 32 * m, head = u >> 3, c = u & 7;
       if (head >= kQHeads && !kv_ok) continue;
       uint4 y1, y2;
-      rotate8(x1[m], x2[m], &s_cos[warp][8 * c], &s_sin[warp][8 * c], y1, y2);
+      rotate8(x1[m], x2[m], tc, ts, y1, y2);
       uint4* dst = head < kQHeads ? qdst + head * 16 : kdst + (head - kQHeads) * 16;
       dst[c] = y1;
       dst[c + 8] = y2;
@@ -155,7 +180,8 @@ using namespace grok;
 static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
                                  const int32_t* start_pos, int B, int T, int Tmax, grok_bf16* q_rot,
                                  grok_bf16* cache_k, grok_bf16* cache_v, PageMap pm, int32_t* dev_status,
-                                 void* stream, const char* name) {
+                                 void* stream, const char* name, const float* cos_tab = nullptr,
+                                 const float* sin_tab = nullptr, int tab_n = 0) {
   if (!q || !k || !v || !start_pos || !q_rot || !cache_k || !cache_v)
     return fail(GROK_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(cache_k) ||
@@ -173,17 +199,23 @@ static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const g
   while (team < 8 && ntok * team * 2 <= (long long)sms * 4 * kRopeWarps) team *= 2;
   const long long want = (ntok * team + kRopeWarps - 1) / kRopeWarps;
   const int grid = int(want < (long long)sms * 8 ? want : (long long)sms * 8);
-  auto kernel = team == 8 ? rope_kv_append_kernel<8>
-               : team == 4 ? rope_kv_append_kernel<4>
-               : team == 2 ? rope_kv_append_kernel<2>
-                           : rope_kv_append_kernel<1>;
+  const bool tab = cos_tab != nullptr;
+  auto kernel = tab ? (team == 8   ? rope_kv_append_kernel<8, true>
+                       : team == 4 ? rope_kv_append_kernel<4, true>
+                       : team == 2 ? rope_kv_append_kernel<2, true>
+                                   : rope_kv_append_kernel<1, true>)
+                    : (team == 8   ? rope_kv_append_kernel<8, false>
+                       : team == 4 ? rope_kv_append_kernel<4, false>
+                       : team == 2 ? rope_kv_append_kernel<2, false>
+                                   : rope_kv_append_kernel<1, false>);
   // Few tokens (a decode step): the SMs' shared-memory split is set for the
   // decode kernel that may join them, not for this kernel's 2 KB.
   static bool carve_set[kMaxDevices] = {};  // per device; idempotent: every thread would set the same values
   int dev = 0;
   if ((st = device_index(&dev)) != GROK_OK) return st;
   if (!carve_set[dev]) {
-    for (auto kf : {rope_kv_append_kernel<8>, rope_kv_append_kernel<4>, rope_kv_append_kernel<2>}) {
+    for (auto kf : {rope_kv_append_kernel<8, false>, rope_kv_append_kernel<4, false>, rope_kv_append_kernel<2, false>,
+                    rope_kv_append_kernel<8, true>, rope_kv_append_kernel<4, true>, rope_kv_append_kernel<2, true>}) {
       cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout,
                                            int(cudaSharedmemCarveoutMaxShared));
       if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -193,8 +225,23 @@ static grok_status append_launch(const grok_bf16* q, const grok_bf16* k, const g
   kernel<<<grid, kRopeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
       start_pos, B, T, Tmax, reinterpret_cast<uint4*>(q_rot), reinterpret_cast<uint4*>(cache_k),
-      reinterpret_cast<uint4*>(cache_v), pm, dev_status);
+      reinterpret_cast<uint4*>(cache_v), pm, reinterpret_cast<const float4*>(cos_tab),
+      reinterpret_cast<const float4*>(sin_tab), tab_n, dev_status);
   return check_launch("rope_kv_append");
+}
+
+extern "C" grok_status grok_rope_kv_append_table(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                                 const int32_t* start_pos, int B, int T, int Tmax,
+                                                 const float* cos_tab, const float* sin_tab, int tab_positions,
+                                                 grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v,
+                                                 int32_t* dev_status, void* stream) {
+  if (!cos_tab || !sin_tab) return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append_table: null table");
+  if (!aligned16(cos_tab) || !aligned16(sin_tab))
+    return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append_table: tables must be 16-byte aligned");
+  if (tab_positions < 1 || tab_positions > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_rope_kv_append_table: need 1 <= tab_positions <= %d", GROK_MAX_POSITION);
+  return append_launch(q, k, v, start_pos, B, T, Tmax, q_rot, cache_k, cache_v, PageMap{nullptr, 0, 0}, dev_status,
+                       stream, "grok_rope_kv_append_table", cos_tab, sin_tab, tab_positions);
 }
 
 extern "C" grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,

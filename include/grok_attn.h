@@ -17,7 +17,8 @@
  *     §6.6.2         paged KV cache (pages allocated only when used)
  *
  * Calls by group:
- *   attention core      grok_rope_kv_append, grok_rope_cos_sin, grok_attn_prefill,
+ *   attention core      grok_rope_kv_append, grok_rope_kv_append_table, grok_rope_cos_sin,
+ *                       grok_attn_prefill,
  *                       grok_attn_prefill_workspace, grok_attn_prefill_ws,
  *                       grok_attn_decode_workspace, grok_attn_decode, grok_attn_combine,
  *                       grok_attn_decode_step_static, grok_attn_decode_step(_workspace)
@@ -135,6 +136,22 @@ grok_status grok_rope_kv_append(const grok_bf16* q, const grok_bf16* k, const gr
                                 grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status, void* stream);
 
 /*
+ * grok_rope_kv_append with the (cos, sin) pairs read from a table instead of
+ * evaluated per token. The values depend only on the position (ch. 4 §4.3.1),
+ * so one table, filled once by grok_rope_cos_sin(0, tab_positions, cos_tab,
+ * sin_tab), serves every layer and every step of a model: the per-layer
+ * append then does no transcendental work. Same bits as grok_rope_kv_append.
+ *   cos_tab, sin_tab: device float[tab_positions * 64] (position p, frequency j
+ *   at p * 64 + j), 16-byte aligned; positions start_pos[b] + T must not exceed
+ *   tab_positions (else GROK_DEV_BAD_START and the sequence is skipped).
+ * Other arguments as for grok_rope_kv_append.
+ */
+grok_status grok_rope_kv_append_table(const grok_bf16* q, const grok_bf16* k, const grok_bf16* v,
+                                      const int32_t* start_pos, int B, int T, int Tmax, const float* cos_tab,
+                                      const float* sin_tab, int tab_positions, grok_bf16* q_rot, grok_bf16* cache_k,
+                                      grok_bf16* cache_v, int32_t* dev_status, void* stream);
+
+/*
  * The fp32 RoPE table the append uses (ch. 4 §4.3.1: phase = t * inv_freq,
  * cos and sin of it): cos_out[i * 64 + j] and sin_out[i * 64 + j] for position
  * first_position + i and frequency j < 64, i < n_positions; each value is the
@@ -176,15 +193,21 @@ grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k, 
  * handled; results then equal grok_attn_prefill's for those items.
  *   workspace: caller-owned device memory, 256-byte aligned, of at least
  *   grok_attn_prefill_workspace(B, Tmax) bytes (B * round_up(Tmax, 128) * 2 KB
- *   for the V copy plus a header of about B * Tmax / 128 * 864 bytes); it holds
- *   nothing between calls, and calls that overlap on the GPU need separate
- *   workspaces.
+ *   for the V copy plus a header of about B * Tmax / 128 * 864 bytes). Calls
+ *   that overlap on the GPU need separate workspaces.
+ *   reuse_v_half: 0 = convert rows [0, start_pos[b] + T) (the call is self-
+ *   contained). 1 = convert only rows [start_pos[b], start_pos[b] + T): rows
+ *   below start_pos[b] must already be in this workspace from earlier calls
+ *   over the same caches (for example the previous chunks of a chunked
+ *   prefill), and no other call may have written those cache rows since (a
+ *   decode step's append, a slot insertion); a sequence once found to hold V
+ *   beyond fp16 stays on the bf16 path until a call with 0.
  */
 grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes);
 grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
                                  const int32_t* start_pos, const int32_t* valid_len, int B, int T, int Tmax,
-                                 grok_bf16* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                 void* stream);
+                                 grok_bf16* out, void* workspace, size_t workspace_bytes, int reuse_v_half,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * Bytes of device workspace grok_attn_decode needs for B sequences and a cache
@@ -373,11 +396,12 @@ grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const i
  *   [B,Tmax,8,128] bf16 (16-byte aligned): every step appends to them and
  *   attends over them, and they must stay allocated until destroy. Allocates
  *   about B*T*(5*48 + 4*8)*128*2 bytes of device memory on the current device,
- *   plus grok_attn_prefill_workspace(B, Tmax) bytes, which the pipeline uses
- *   from then on. *pipe receives the handle.
+ *   plus grok_attn_prefill_workspace(B, Tmax) bytes and a Tmax * 512-byte
+ *   cos/sin table, which the pipeline uses from then on. *pipe receives the handle.
  * grok_prefill_pipe_submit: queue one step. Copy q [B,T,48,128], k and v
  *   [B,T,8,128], start_pos [B] and valid_len [B] (NULL: every token valid) from
- *   host memory; run grok_rope_kv_append then grok_attn_prefill_ws; copy the output
+ *   host memory; run grok_rope_kv_append_table (with a cos/sin table of
+ *   positions [0, Tmax) made at create) then grok_attn_prefill_ws; copy the output
  *   [B,T,48,128] to host memory at out. Returns once the work is queued. The
  *   host buffers must stay valid, the inputs unchanged and the output unread
  *   until the next grok_prefill_pipe_wait. Page-locked host memory

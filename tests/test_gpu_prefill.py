@@ -181,3 +181,34 @@ def test_prefill_bad_integers_set_status(impl):
     inp = W.custom(B=2, T=16, Tmax=32, start_pos=[0, 8], valid_len=[16, 0], seed=25)
     *_, status = run_prefill(inp, impl=impl)
     assert status & G.DEV_BAD_VALID
+
+
+def test_prefill_ws_reusing_the_fp16_copy_across_chunks():
+    """A chunked prefill in two calls on one workspace: the second call converts only its
+    own 300 rows of V (reuse_v_half) and must give the same bits as a call that converts
+    every row, and match the oracle."""
+    import grok_gqa_attention_gb300 as G
+    dev = "cuda"
+    B, Tmax = 2, 1024
+    first = W.custom(B=B, T=300, Tmax=Tmax, start_pos=[0, 0], valid_len=[300, 300], seed=31)
+    second = W.custom(B=B, T=300, Tmax=Tmax, start_pos=[300, 300], valid_len=[300, 211], seed=32)
+    ck, cv = first.cache_k.to(dev), first.cache_v.to(dev)
+    ws = G.alloc_prefill_workspace(B, Tmax, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = []
+    for inp, reuse in ((first, False), (second, True)):
+        q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+        start, valid = inp.start_pos.to(dev), inp.valid_len.to(dev)
+        q_rot, out = torch.empty_like(q), torch.empty_like(q)
+        G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+        G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status, reuse_v_half=reuse)
+        outs.append((q_rot, start, valid, out))
+    q_rot, start, valid, out = outs[1]
+    full = torch.empty_like(out)
+    G.prefill_ws(q_rot, ck, cv, start, valid, full, G.alloc_prefill_workspace(B, Tmax, dev), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+    ref = A.attention(W.bits(q_rot.cpu()), W.bits(ck.cpu()), W.bits(cv.cpu()), second.start_pos.numpy(),
+                      second.valid_len.numpy())
+    assert_close(W.bits(out.cpu()), ref, "second chunk, reused fp16 V")

@@ -78,3 +78,40 @@ def test_cos_sin_table_bit_exact_for_every_supported_position():
     oc, os_ = R.cos_sin(R.phase(t, R.inv_freq(128)))
     assert np.array_equal(c.cpu().numpy().view(np.uint32), oc[0].view(np.uint32))
     assert np.array_equal(s.cpu().numpy().view(np.uint32), os_[0].view(np.uint32))
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_append_from_table_bit_exact_at_full_size(name):
+    """The table variant (cos/sin from a table of every position, filled once) writes the
+    same bits as the oracle on every workload."""
+    import grok_gqa_attention_gb300 as G
+    inp = cached_inputs(name)
+    dev = "cuda"
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    q_rot = torch.empty_like(q)
+    ctab, stab = G.rope_cos_sin(0, inp.workload.Tmax)
+    G.rope_kv_append_table(q, k, v, start, ctab, stab, q_rot, ck, cv, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    oq, ok_, ov = oracle_append(inp)
+    assert np.array_equal(W.bits(q_rot.cpu()), oq)
+    assert np.array_equal(W.bits(ck.cpu()), ok_)
+    assert np.array_equal(W.bits(cv.cpu()), ov)
+
+
+def test_append_from_table_positions_beyond_the_table_set_status():
+    import grok_gqa_attention_gb300 as G
+    inp = W.custom(B=2, T=8, Tmax=64, start_pos=[4, 40], seed=7)
+    dev = "cuda"
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ctab, stab = G.rope_cos_sin(0, 32)          # covers positions [0, 32): sequence 1 needs 40..47
+    G.rope_kv_append_table(q, k, v, start, ctab, stab, torch.empty_like(q), ck, cv, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & G.DEV_BAD_START
+    assert np.array_equal(W.bits(ck.cpu())[1], W.bits(inp.cache_k)[1])   # untouched
