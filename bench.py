@@ -538,9 +538,15 @@ def run_other_prefill(args, rank, world, dist, dev, peaks, peak_kind):
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         ws = G.alloc_prefill_workspace(w.B, w.Tmax, dev)
         flops = prefill_flops(inp.start_pos.numpy(), valid_np, w.T)
-        calls = {"append": lambda: G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status),
+        cos_tab, sin_tab = G.rope_cos_sin(0, w.Tmax)
+        calls = {"append": lambda: G.rope_kv_append_table(q, k, v, start, cos_tab, sin_tab, q_rot, ck, cv, status),
                  "prefill_ws": lambda: G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status),
                  "prefill_bf16_weights": lambda: G.prefill(q_rot, ck, cv, start, valid, out, status)}
+        if name.startswith("chunked"):
+            # steady state of a chunked prefill: the cached rows were converted by the calls
+            # that appended them, so each call converts only its own 256 rows per sequence
+            calls["prefill_ws_reusing_v_half"] = lambda: G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status,
+                                                                      reuse_v_half=True)
         times = {}
         for key, fn in calls.items():
             for _ in range(args.warmup):
@@ -569,10 +575,14 @@ def run_other_prefill(args, rank, world, dist, dev, peaks, peak_kind):
                       for b, n in enumerate(valid_np))
             entry["algorithmic_gflop_valid_rows_only"] = 48.0 * 4 * 128 * vis / 1e9
         if name.startswith("chunked"):
-            entry["note"] = ("the call converts every cached V row [0, start + T) to fp16 each time "
-                             "(6400 rows per sequence here), part of the measured prefill time")
+            entry["note"] = ("prefill_ws converts every cached V row [0, start + T) to fp16 each call (6400 rows "
+                             "per sequence); prefill_ws_reusing_v_half converts only the chunk's rows, the rest "
+                             "being in the workspace from the calls that appended them")
+            entry["prefill_reusing_v_half_TFLOP/s"] = flops / (ms["prefill_ws_reusing_v_half"] * 1e-3) / 1e12
+            entry["roofline_reusing_v_half"] = {"bound": "tensor", "frac": entry["prefill_reusing_v_half_TFLOP/s"] / peak_tf,
+                                                "peak": peak_tf, "peak_source": f"bf16_tflops ({peak_kind})"}
         res[name] = entry
-        del q, k, v, ck, cv, q_rot, out, ws
+        del q, k, v, ck, cv, q_rot, out, ws, cos_tab, sin_tab
         torch.cuda.empty_cache()
     return res
 
@@ -711,7 +721,10 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
         return m, t
 
     ms_plain, t_plain = timed(lambda: G.qkv_project(x2d, w, y))
-    ms_fused, t_fused = timed(lambda: G.qkv_rope_append(x, w, start, q_rot, ck, cv, ws, status))
+    ms_fused_step_table, t_fused_step_table = timed(lambda: G.qkv_rope_append(x, w, start, q_rot, ck, cv, ws, status))
+    # the same with a cos/sin table of every position computed once (shared by all layers and steps)
+    cos_tab, sin_tab = G.rope_cos_sin(0, Tmax)
+    ms_fused, t_fused = timed(lambda: G.qkv_rope_append_table(x, w, start, cos_tab, sin_tab, q_rot, ck, cv, status))
     ms_cublas, _ = timed(lambda: torch.matmul(x2d, w))
     # output projection (the step after the attention call): [M, 6144] . W_o [6144, 6144]
     gen = torch.Generator().manual_seed(100 + rank)
@@ -773,9 +786,14 @@ def run_qkv(args, rank, world, dist, dev, peaks, peak_kind):
         "workload": f"qkv_b{B}_t{T}", "shape": {"M": M, "K": G.MODEL_SIZE, "N": G.QKV_COLUMNS},
         "metric": "Q/K/V projection TFLOP/s (2*M*K*N per step)",
         "value": whole_job_rate(flops, world, ms_fused, 1e12), "unit": "TFLOP/s", "ms_per_step": ms_fused,
-        "step": "grok_qkv_rope_append: cos/sin table kernel + projection GEMM with RoPE and cache-append epilogue",
+        "step": ("grok_qkv_rope_append_table: projection GEMM with RoPE and cache-append epilogue, cos/sin from "
+                 "a table of every position computed once before timing"),
         "plain": {"ms": ms_plain, "TFLOP/s": tf_plain, "stats": time_stats(t_plain)},
         "fused_stats": time_stats(t_fused),
+        "fused_frac": flops / (ms_fused * 1e-3) / 1e12 / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+        "fused_with_per_call_table": {"call": "grok_qkv_rope_append (table kernel + GEMM, programmatic dependent)",
+                                      "ms": ms_fused_step_table, "stats": time_stats(t_fused_step_table),
+                                      "TFLOP/s": flops / (ms_fused_step_table * 1e-3) / 1e12},
         "roofline": {"bound": "tensor", "kernel": "qkv_kernel (plain epilogue, one launch)", "achieved": tf_plain,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": tf_plain / peak_tf,
                      "peak_source": f"bf16_tflops ({peak_kind})", "traffic": measured_traffic("qkv_kernel"),

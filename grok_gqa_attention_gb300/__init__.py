@@ -59,6 +59,7 @@ EXPORTS = (
     "grok_qkv_project",
     "grok_qkv_workspace",
     "grok_qkv_rope_append",
+    "grok_qkv_rope_append_table",
     "grok_linear",
     "grok_dequant_int8",
     "grok_linear_int8_workspace",
@@ -132,6 +133,8 @@ def load() -> ctypes.CDLL:
     lib.grok_qkv_workspace.argtypes = [I, I, ctypes.POINTER(S)]
     lib.grok_qkv_rope_append.restype = I
     lib.grok_qkv_rope_append.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P, P]
+    lib.grok_qkv_rope_append_table.restype = I
+    lib.grok_qkv_rope_append_table.argtypes = [P, P, P, I, I, I, P, P, I, P, P, P, P, P]
     lib.grok_linear.restype = I
     lib.grok_linear.argtypes = [P, P, I, I, I, P, P, P]
     lib.grok_dequant_int8.restype = I
@@ -445,6 +448,27 @@ def qkv_rope_append(x, w, start_pos, q_rot, cache_k, cache_v, workspace, dev_sta
     _check(load().grok_qkv_rope_append(_ptr(x), _ptr(w), _ptr(start_pos), B, T, Tmax, _ptr(q_rot), _ptr(cache_k),
                                        _ptr(cache_v), _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                        _stream(stream)))
+
+
+def qkv_rope_append_table(x, w, start_pos, cos_tab, sin_tab, q_rot, cache_k, cache_v, dev_status=None,
+                          stream=None) -> None:
+    """qkv_rope_append with cos/sin from a table of positions [0, n) (see grok_qkv_rope_append_table)."""
+    B, T = x.shape[0], x.shape[1]
+    Tmax = cache_k.shape[1]
+    n = cos_tab.shape[0]
+    _want(x, "x", torch.bfloat16, (B, T, MODEL_SIZE))
+    _want(w, "w", torch.bfloat16, (MODEL_SIZE, QKV_COLUMNS))
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    _want(cos_tab, "cos_tab", torch.float32, (n, 64))
+    _want(sin_tab, "sin_tab", torch.float32, (n, 64))
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(cache_k, "cache_k", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    _want(cache_v, "cache_v", torch.bfloat16, (B, Tmax, N_KV_HEADS, HEAD_DIM))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_qkv_rope_append_table(_ptr(x), _ptr(w), _ptr(start_pos), B, T, Tmax, _ptr(cos_tab),
+                                             _ptr(sin_tab), n, _ptr(q_rot), _ptr(cache_k), _ptr(cache_v),
+                                             _ptr(dev_status), _stream(stream)))
 
 
 def linear(x, w, y, dev_status=None, stream=None) -> None:

@@ -73,8 +73,9 @@ constexpr int kQkvSmem = kQkvStages * kQkvStageBytes + int(sizeof(QkvBars)) + 10
 struct QkvParams {
   int M, K, N, T, Tmax, n_mtiles, n_ntiles, k_blocks, n_tiles;
   const int32_t* start_pos;     // fused epilogue only
-  const float* cos_tab;         // [M][64]
+  const float* cos_tab;         // [M][64] per token row, or [tab_n][64] per position (tab_n > 0)
   const float* sin_tab;
+  int tab_n;                    // > 0: the tables hold positions [0, tab_n), indexed by position
   uint4* y;                     // plain: [M][N]
   uint4* q_rot;                 // fused: [B][T][48][128]
   uint4* cache_k;               // fused: [B][Tmax][8][128]
@@ -320,7 +321,11 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       } else {
         const int b = row / p.T, i = row % p.T;
         const int s = live ? __ldg(p.start_pos + b) : 0;
-        const bool write = live && s >= 0 && (long long)s + p.T <= p.Tmax;
+        const bool write = live && s >= 0 && (long long)s + p.T <= p.Tmax &&
+                           (p.tab_n == 0 || (long long)s + p.T <= p.tab_n);
+        // with a position table no table kernel runs to report a bad start: the epilogue does
+        if (live && i == 0 && !write && p.tab_n > 0) report(p.status, GROK_DEV_BAD_START);
+        const size_t trow = p.tab_n > 0 ? (size_t)(s + i) : (size_t)row;  // table row of this token
         // cache row of position s + i: contiguous b * Tmax + s + i; paged page * 128 + (s + i) % 128
         size_t crow = (size_t)b * p.Tmax + s + i;
         bool kv_write = write;
@@ -357,8 +362,8 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
             qkv_round32(a, x2);
             if (rotate && write) {
               float cs[32], sn[32];
-              const float4* cp = reinterpret_cast<const float4*>(p.cos_tab + (size_t)row * 64 + c * 32);
-              const float4* sp = reinterpret_cast<const float4*>(p.sin_tab + (size_t)row * 64 + c * 32);
+              const float4* cp = reinterpret_cast<const float4*>(p.cos_tab + trow * 64 + c * 32);
+              const float4* sp = reinterpret_cast<const float4*>(p.sin_tab + trow * 64 + c * 32);
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
                 const float4 cv = __ldg(cp + q), sv = __ldg(sp + q);
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kDqThreads) dequant_int8_kernel(const uint4* _
 
 
 grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M, int K, int N, QkvParams& prm,
-                       void* stream) {
+                       void* stream, bool after_table = true) {
   int sms = 0;
   grok_status st = device_sm_count(&sms);
   if (st != GROK_OK) return st;
@@ -487,7 +492,7 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the table kernel before it
-  attr[0].val.programmaticStreamSerializationAllowed = fused ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = (fused && after_table) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, prm);
@@ -580,6 +585,40 @@ static grok_status qkv_rope_append_launch(const grok_bf16* x, const grok_bf16* w
   grok_status st = check_launch("qkv table");
   if (st != GROK_OK) return st;
   return qkv_launch(true, x, w, int(M), kQkvK, kQkvN, prm, stream);
+}
+
+// The fused projection with cos/sin from a table of positions [0, tab_n)
+// (grok_rope_cos_sin(0, tab_n)): no per-call table kernel and no workspace.
+extern "C" grok_status grok_qkv_rope_append_table(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos,
+                                                  int B, int T, int Tmax, const float* cos_tab, const float* sin_tab,
+                                                  int tab_positions, grok_bf16* q_rot, grok_bf16* cache_k,
+                                                  grok_bf16* cache_v, int32_t* dev_status, void* stream) {
+  const char* name = "grok_qkv_rope_append_table";
+  if (!x || !w || !start_pos || !q_rot || !cache_k || !cache_v || !cos_tab || !sin_tab)
+    return fail(GROK_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned16(x) || !aligned16(w) || !aligned32(q_rot) || !aligned32(cache_k) || !aligned32(cache_v) ||
+      !aligned16(cos_tab) || !aligned16(sin_tab))
+    return fail(GROK_ERR_INVALID_ARG, "%s: x, w and the tables must be 16-byte aligned, q_rot and the caches "
+                "32-byte aligned", name);
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION || tab_positions < 1 ||
+      tab_positions > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "%s: need B >= 1, 1 <= T <= Tmax <= %d, 1 <= tab_positions <= %d", name,
+                GROK_MAX_POSITION, GROK_MAX_POSITION);
+  const long long M = (long long)B * T;
+  if (M > (1LL << 30)) return fail(GROK_ERR_INVALID_ARG, "%s: B * T too large", name);
+  QkvParams prm = {};
+  prm.T = T;
+  prm.Tmax = Tmax;
+  prm.start_pos = start_pos;
+  prm.cos_tab = cos_tab;
+  prm.sin_tab = sin_tab;
+  prm.tab_n = tab_positions;
+  prm.q_rot = reinterpret_cast<uint4*>(q_rot);
+  prm.cache_k = reinterpret_cast<uint4*>(cache_k);
+  prm.cache_v = reinterpret_cast<uint4*>(cache_v);
+  prm.pm = PageMap{nullptr, 0, 0};
+  prm.status = dev_status;
+  return qkv_launch(true, x, w, int(M), kQkvK, kQkvN, prm, stream, false);
 }
 
 extern "C" grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,

@@ -23,7 +23,8 @@
  *                       grok_attn_decode_workspace, grok_attn_decode, grok_attn_combine,
  *                       grok_attn_decode_step_static, grok_attn_decode_step(_workspace)
  *   projections         grok_qkv_project, grok_linear, grok_dequant_int8,
- *                       grok_linear_int8(_workspace), grok_qkv_workspace, grok_qkv_rope_append
+ *                       grok_linear_int8(_workspace), grok_qkv_workspace, grok_qkv_rope_append,
+ *                       grok_qkv_rope_append_table
  *   runtime             grok_prefill_pipe_create / _submit / _wait / _destroy
  *   paged cache         grok_rope_kv_append_paged, grok_attn_prefill_paged,
  *                       grok_attn_decode_paged, grok_qkv_rope_append_paged
@@ -379,6 +380,19 @@ grok_status grok_linear_int8_workspace(int K, int N, size_t* bytes);
 grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, const float* scales, int M, int K, int N,
                              grok_bf16* y, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 grok_status grok_qkv_workspace(int B, int T, size_t* bytes);
+/*
+ * grok_qkv_rope_append with cos/sin read from a table of positions
+ * [0, tab_positions) (grok_rope_cos_sin(0, tab_positions, ...), filled once
+ * and shared by every layer and step) instead of a per-call table: no table
+ * kernel and no workspace. Same bits as grok_qkv_rope_append. A sequence whose
+ * positions start_pos[b] + T exceed Tmax or tab_positions sets
+ * GROK_DEV_BAD_START and none of its rows are written. cos_tab, sin_tab:
+ * device float[tab_positions * 64], 16-byte aligned.
+ */
+grok_status grok_qkv_rope_append_table(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B,
+                                       int T, int Tmax, const float* cos_tab, const float* sin_tab, int tab_positions,
+                                       grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v, int32_t* dev_status,
+                                       void* stream);
 grok_status grok_qkv_rope_append(const grok_bf16* x, const grok_bf16* w, const int32_t* start_pos, int B, int T,
                                  int Tmax, grok_bf16* q_rot, grok_bf16* cache_k, grok_bf16* cache_v, void* workspace,
                                  size_t ws_bytes, int32_t* dev_status, void* stream);

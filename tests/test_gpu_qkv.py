@@ -78,6 +78,37 @@ def test_fused_equals_rope_append_of_own_projection(small):
     assert np.array_equal(W.bits(cv.cpu()), rv)
 
 
+def test_fused_from_position_table_equals_fused(small):
+    """The fused projection reading a table of every position (no per-call table kernel)
+    writes the same bits as the per-call-table version; a sequence beyond the table is
+    reported and left unwritten."""
+    B, T = small.x.shape[0], small.x.shape[1]
+    Tmax = small.cache_k.shape[1]
+    x, w = small.x.cuda(), small.w.cuda()
+    start = small.start_pos.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ck1, cv1 = small.cache_k.cuda(), small.cache_v.cuda()
+    q1 = torch.empty((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    G.qkv_rope_append(x, w, start, q1, ck1, cv1, G.alloc_qkv_workspace(B, T), status)
+    ck2, cv2 = small.cache_k.cuda(), small.cache_v.cuda()
+    q2 = torch.empty_like(q1)
+    ctab, stab = G.rope_cos_sin(0, Tmax)
+    G.qkv_rope_append_table(x, w, start, ctab, stab, q2, ck2, cv2, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+    assert torch.equal(ck1.view(torch.int16), ck2.view(torch.int16))
+    assert torch.equal(cv1.view(torch.int16), cv2.view(torch.int16))
+    # a table covering positions [0, 250): sequence 0 (start 100, T 200) needs up to 299
+    ck3, cv3 = small.cache_k.cuda(), small.cache_v.cuda()
+    ctab3, stab3 = G.rope_cos_sin(0, 250)
+    G.qkv_rope_append_table(x, w, start, ctab3, stab3, torch.empty_like(q1), ck3, cv3, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & G.DEV_BAD_START
+    assert np.array_equal(W.bits(ck3.cpu())[0], W.bits(small.cache_k)[0])   # sequence 0 untouched
+    assert torch.equal(ck3[1].view(torch.int16), ck2[1].view(torch.int16))   # sequence 1 (start 37) written
+
+
 def test_fused_full_size_sampled_rows():
     B, T, Tmax = 1, 8192, 8192
     inp = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[0], seed=51)
