@@ -138,6 +138,25 @@ def test_prefill_row_maximum_rises_across_tiles(impl):
     _full_check(inp, "rising maximum", impl)
 
 
+def test_prefill_ws_hands_overflowing_items_to_the_bf16_pass():
+    """In the rising-maximum case every row from 256 on sees keys whose capped logits reach
+    about +-30 while its first tile's stay near 0: a rise of about 43 octaves, so its weights
+    would overflow fp16, its item goes on the fallback list and the bf16 pass recomputes it:
+    those rows equal grok_attn_prefill's output bit for bit. The first query tile (rows 0..127
+    see only the small keys) stays on the fp16 path."""
+    inp = W.custom(B=1, T=400, Tmax=512, start_pos=[0], seed=26, scale=3.0)
+    k = inp.k.float()
+    k[:, :128] *= 0.02
+    k[:, 128:256] *= 0.7
+    k[:, 256:] *= 4.0
+    inp.k.copy_(k.to(torch.bfloat16))
+    _, _, _, out16, st16 = run_prefill(inp, impl="f16p")
+    _, _, _, outb, stb = run_prefill(inp, impl="bf16p")
+    assert st16 == 0 and stb == 0
+    assert np.array_equal(out16[0, 256:], outb[0, 256:])
+    assert not np.array_equal(out16[0, :128], outb[0, :128])
+
+
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
 def test_prefill_values_beyond_fp16_range(impl):
     """V values above fp16's largest finite value (65504) in one sequence: the fp16
