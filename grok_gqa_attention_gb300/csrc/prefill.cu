@@ -233,32 +233,74 @@ __device__ __forceinline__ void pf_issue_pv_half(uint32_t d, uint32_t pbase, uin
   }
 }
 
+// tanh(y) for a pair of |y| <= 1.5 on the FMA pipe instead of the special-
+// function unit: the odd polynomial y + y^3 Q(y^2), Q of degree 5, fitted here
+// for absolute error on [0, 1.5] by Lawson's iteratively reweighted least
+// squares (which converges to the minimax fit), then rounded to fp32: maximum
+// absolute error 3.0e-6 including the fp32 steps (tanh.approx: 7.8e-6). The
+// caller checks the range: beyond it the polynomial leaves [-1, 1] quickly.
+constexpr float kTanhPolyRange = 1.5f;
+__device__ __forceinline__ uint64_t tanh_poly_f2(uint64_t y) {
+  const uint64_t z = f2_mul(y, y);
+  const uint64_t yz = f2_mul(y, z);
+  uint64_t q = f2_fma(f2_pack(0x1.38efe80p-12f, 0x1.38efe80p-12f), z, f2_pack(-0x1.999c920p-9f, -0x1.999c920p-9f));
+  q = f2_fma(q, z, f2_pack(0x1.f398040p-7f, 0x1.f398040p-7f));
+  q = f2_fma(q, z, f2_pack(-0x1.9526880p-5f, -0x1.9526880p-5f));
+  q = f2_fma(q, z, f2_pack(0x1.0ddb2e0p-3f, 0x1.0ddb2e0p-3f));
+  q = f2_fma(q, z, f2_pack(-0x1.55208c0p-2f, -0x1.55208c0p-2f));
+  return f2_fma(yz, q, y);
+}
+
 // Column pairs of a 32-key chunk whose exp2 runs on the FMA pipe (bit e: pair
 // e); the rest use the special-function unit, which also evaluates every tanh.
 // Half is best in both modes (fp16 mode: 0.668 ms with half, 0.706 with three
 // quarters, 0.747 with all on prefill_b1_t8192).
 constexpr uint32_t kPolyPairs = 0x3333;
 
+// For a chunk whose logits all lie in the tanh polynomial's range, per mode:
+// the column pairs whose tanh runs as that polynomial on the FMA pipe, and the
+// pairs whose exp2 does (the rest on the special-function unit). Measured on
+// prefill_b1_t8192: fp16 mode 0.661 ms with half the tanh on the polynomial and
+// every exp2 on the special-function unit, against 0.666 with the plain split
+// above (0.674-0.679 with a quarter, 0.690 / 0.710 / 0.780 with five eighths,
+// three quarters, all). bf16 mode has the FMA pipe busier (the lo half of P):
+// every split tried was slower there (0.765-0.85 against 0.750), so it has none.
+constexpr uint32_t kTanhPolyPairsBf16 = 0x0000, kTanhPolyExp2PairsBf16 = 0x0000;
+constexpr uint32_t kTanhPolyPairsF16 = 0x5555, kTanhPolyExp2PairsF16 = 0x0000;
+// Raw logit bound of the polynomial's range |s * kY| <= kTanhPolyRange.
+constexpr float kTanhPolyRaw = kTanhPolyRange / kY;
+
 // S -> P for one 32-key chunk c of one row (this thread's TMEM lane): weights
 // 2^(30 log2(e) tanh(y) - mref) (mref = 30 log2(e): exp(capped logit - 30)),
 // zero where masked, accumulated into the row sum and returned as bf16 hi/lo
 // halves for the caller to write back over S (keys 32c..32c+31: hi in columns
 // 32c..32c+15, lo in 32c+16..32c+31), or in fp16 mode as fp16 pairs (hi only).
-template <bool kMask, bool kF16>
+// kTanhPoly (fp16 mode, every logit of the warp's chunk within kTanhPolyRaw):
+// the tanh of the pairs in kTanhPolyPairs is the FMA-pipe polynomial.
+template <bool kMask, bool kF16, bool kTanhPoly>
 __device__ __forceinline__ void pf_softmax_chunk(const uint32_t (&sv)[32], int c, int rel, float mref, float& l0,
                                                  float& l1, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
   // The arithmetic of capped_weight and split_bf16x2, two columns at a time
-  // with packed f32x2 instructions; the exp2 of the pairs in kPolyPairs is the
-  // FMA-pipe polynomial instead of ex2.approx.
+  // with packed f32x2 instructions; the exp2 of the pairs in the exp2 mask is
+  // the FMA-pipe polynomial instead of ex2.approx.
+  constexpr uint32_t exp2_pairs = !kTanhPoly ? kPolyPairs : kF16 ? kTanhPolyExp2PairsF16 : kTanhPolyExp2PairsBf16;
+  constexpr uint32_t tanh_pairs = !kTanhPoly ? 0u : kF16 ? kTanhPolyPairsF16 : kTanhPolyPairsBf16;
   const uint64_t y2 = f2_pack(kY, kY), t2 = f2_pack(kT, kT), mt2 = f2_pack(-mref, -mref);
   uint64_t l = f2_pack(l0, l1);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float y0, y1, x0, x1;
-    f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), y2), y0, y1);
-    const uint64_t x = f2_fma(f2_pack(tanh_approx(y0), tanh_approx(y1)), t2, mt2);
+    const uint64_t y = f2_mul(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), y2);
+    uint64_t t;
+    if ((tanh_pairs >> e) & 1) {
+      t = tanh_poly_f2(y);
+    } else {
+      f2_unpack(y, y0, y1);
+      t = f2_pack(tanh_approx(y0), tanh_approx(y1));
+    }
+    const uint64_t x = f2_fma(t, t2, mt2);
     float w0, w1;
-    if ((kPolyPairs >> e) & 1) {
+    if ((exp2_pairs >> e) & 1) {
       exp2_poly_f2(x, w0, w1);
     } else {
       f2_unpack(x, x0, x1);
@@ -304,7 +346,26 @@ __device__ __forceinline__ void pf_softmax_half(uint32_t trow, int half, int rel
     uint32_t hi[16], lo[16];
     tmem_ld32(trow + c * 32, a);
     tmem_wait_ld_dep(a);
-    pf_softmax_chunk<kMask, kF16>(a, c, rel, mref, l0, l1, hi, lo);
+    constexpr uint32_t tanh_pairs = kF16 ? kTanhPolyPairsF16 : kTanhPolyPairsBf16;
+    if (tanh_pairs != 0 && !kMask) {
+      // The polynomial form only when every logit of the warp's chunk in its
+      // columns is in its range (a warp-uniform choice; fmaxf skips a NaN
+      // logit, which stays NaN through the polynomial as through tanh.approx).
+      // Only whole-visible chunks take it, so that keys behind a mask, whatever
+      // the cache holds there, cannot change which form the visible ones get.
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if ((tanh_pairs >> e) & 1)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(a[2 * e])), fabsf(__uint_as_float(a[2 * e + 1]))));
+      if (__all_sync(0xffffffffu, m <= kTanhPolyRaw)) {
+        pf_softmax_chunk<kMask, kF16, true>(a, c, rel, mref, l0, l1, hi, lo);
+      } else {
+        pf_softmax_chunk<kMask, kF16, false>(a, c, rel, mref, l0, l1, hi, lo);
+      }
+    } else {
+      pf_softmax_chunk<kMask, kF16, false>(a, c, rel, mref, l0, l1, hi, lo);
+    }
     tmem_st16(trow + c * 32, hi);
     if (!kF16) tmem_st16(trow + c * 32 + 16, lo);
   }

@@ -34,7 +34,17 @@ def _caches():
     return base.cache_k, base.cache_v
 
 
-def test_pipeline_matches_step_by_step_device_calls():
+def _host_out(kind):
+    """Host output buffer: page-locked (copies overlap the kernels) or pageable
+    (copies serialise)."""
+    shape = (B, T, 48, 128)
+    if kind == "pinned":
+        return torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    return torch.empty(shape, dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("out_kind", ["pinned", "pageable"])
+def test_pipeline_matches_step_by_step_device_calls(out_kind):
     steps = _steps()
     ck0, cv0 = _caches()
     # reference: device entry points, one step after another
@@ -62,7 +72,7 @@ def test_pipeline_matches_step_by_step_device_calls():
         for inp in steps:
             hin = [inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory(), inp.start_pos.pin_memory(),
                    None if inp.valid_len is None else inp.valid_len.pin_memory()]
-            hout = torch.empty((B, T, 48, 128), dtype=torch.bfloat16).pin_memory()
+            hout = _host_out(out_kind)
             host_in.append(hin)
             host_out.append(hout)
             G.prefill_pipe_submit(pipe, B, T, *hin, hout)

@@ -117,6 +117,28 @@ def test_prefill_saturated_logits(impl):
 
 
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_prefill_tanh_polynomial_range_split(impl):
+    """The fp16 pass takes tanh from an FMA-pipe polynomial for half of a 32-key
+    chunk's columns (pairs 0, 2, 4, ...: columns 0, 1, 4, 5, ...) when no logit
+    of the warp's chunk in those columns exceeds 45 (|y| = 1.5) in magnitude,
+    and tanh.approx otherwise. Keys per 32-key chunk: all small (logits within
+    the range), one large key in a polynomial column, one in a tanh.approx
+    column (the check ignores it), or all large."""
+    inp = W.custom(B=1, T=512, Tmax=512, start_pos=[0], seed=27, scale=2.0)
+    k = inp.k.float()
+    for c in range(512 // 32):
+        kind = c % 4
+        if kind == 1:
+            k[0, 32 * c] *= 10.0
+        elif kind == 2:
+            k[0, 32 * c + 2] *= 10.0
+        elif kind == 3:
+            k[0, 32 * c:32 * c + 32] *= 10.0
+    inp.k.copy_(k.to(torch.bfloat16))
+    _full_check(inp, "tanh polynomial range split", impl)
+
+
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
 def test_prefill_all_weights_tiny(impl):
     """Small inputs with all logits near zero: every weight near exp(-30) relative to the fixed reference."""
     inp = W.custom(B=1, T=192, Tmax=256, start_pos=[0], seed=23, scale=0.05)
@@ -126,9 +148,9 @@ def test_prefill_all_weights_tiny(impl):
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
 def test_prefill_row_maximum_rises_across_tiles(impl):
     """Keys of the first 128-key tile give logits near 0, later keys logits near +-30:
-    a row's maximum rises by up to ~43 octaves after its first tile, so the fp16
-    path must move its reference and rescale O and the row sum (more than once,
-    since the middle tile rises only part of the way)."""
+    a row's maximum rises by up to ~43 octaves after its first tile, far past the
+    fp16 pass's headroom, so that pass lists the overflowing items and the bf16
+    pass recomputes them (the middle tile rises only part of the way)."""
     inp = W.custom(B=1, T=400, Tmax=512, start_pos=[0], seed=26, scale=3.0)
     k = inp.k.float()
     k[:, :128] *= 0.02      # first tile: |logits| ~ 0.2 before the cap
