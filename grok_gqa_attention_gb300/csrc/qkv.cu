@@ -16,13 +16,15 @@
 // serves the output projection [M, 6144] . W_o [6144, 6144] and each
 // tensor-parallel rank's head slice of it.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
+// Persistent kernel, one CTA per SM, 10 warps:
 //   warp 0      TMA producer: per 64-wide K block two X boxes [128 rows x 64]
 //               and four W boxes [64 rows x 64 columns] (64 KB) into a 3-stage
 //               ring
 //   warp 1      TMEM owner and MMA issuer (converged; one fixed lane issues)
-//   warps 2-5   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
-//               row per thread
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
+//               row per thread; of the two warps on a lane quarter, warps 2-5
+//               take the first half of every head's features (fused: 0..31
+//               with their rotation partners 64..95), warps 6-9 the second
 // Tile = 256 rows x 256 columns (two heads), as two 128-row halves that share
 // each staged W block: tcgen05.mma M=128, N=256, K=16 per half, A = X
 // (K-major), B = W (N-contiguous rows, MN-major), both 128-byte swizzled. The
@@ -38,10 +40,16 @@
 // -> cache_k at row start_pos[b] + i, or at its page of a paged pool; v heads
 // -> cache_v). The rotation is the
 // one of rope_kv_append (separately rounded fp32 products and sum of the bf16
-// value and the fp32 cos / sin) with cos / sin taken from a per-step table
-// that qkv_table_kernel fills with the shared fp64 routine. The projection is
+// value and the fp32 cos / sin; scalar instructions, since ptxas may fuse a
+// packed f32x2 multiply into the add that consumes it) with cos / sin taken
+// from a table: per position (grok_qkv_rope_append_table), or per token row,
+// filled by qkv_table_kernel with the shared fp64 routine. The projection is
 // that kernel's programmatic dependent launch: its main loop runs while the
-// table is computed, and its epilogue waits for the table grid.
+// table is computed, and its epilogue waits for the table grid. The half's
+// epilogue holds back the next tile's products, so it stages the table through
+// shared memory (coalesced loads; see kQkvTabWarpBytes) and splits each row
+// over two warps: with per-row table loads it cost 50 us over the plain
+// epilogue, staged and split 27 us.
 #include "common.cuh"
 #include "host.cuh"
 #include "rope_math.cuh"
@@ -53,7 +61,8 @@ constexpr int kQkvN = 8192;                 // 48 * 128 + 2 * 8 * 128
 constexpr int kQkvBM = 256, kQkvBN = 256, kQkvBK = 64;  // tile: two 128-row MMA halves
 constexpr int kQkvHM = 128;                               // rows per MMA and per X box
 constexpr int kQkvStages = 3;
-constexpr int kQkvThreads = 192;
+constexpr int kQkvThreads = 320;
+constexpr int kQkvEpiThreads = 256;  // warps 2-9
 constexpr int kQkvGroupM = 16;  // 256-row blocks per tile group (8: 1 % slower, 32: 1-2 % slower)
 constexpr int kQkvABox = kQkvHM * kQkvBK * 2;               // 16 KB: one half's X block
 constexpr int kQkvABytes = 2 * kQkvABox;                    // 32 KB
@@ -68,7 +77,16 @@ struct QkvBars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kQkvSmem = kQkvStages * kQkvStageBytes + int(sizeof(QkvBars)) + 1024;
+// Fused epilogue: each epilogue warp stages its 32 rows' cos / sin for 16
+// features at a time (4 KB) in shared memory. A row's slice is 64 contiguous
+// bytes of the table, so a warp that loads its own row per thread touches 32
+// lines per load (32 L1 wavefronts); staged, a load reads eight whole row
+// slices (4 wavefronts), and the tile's two heads share them.
+constexpr int kQkvTabWarpBytes = 4096;
+constexpr int kQkvTabBytes = 8 * kQkvTabWarpBytes;
+constexpr int qkv_smem(bool fused) {
+  return kQkvStages * kQkvStageBytes + (fused ? kQkvTabBytes : 0) + int(sizeof(QkvBars)) + 1024;
+}
 
 struct QkvParams {
   int M, K, N, T, Tmax, n_mtiles, n_ntiles, k_blocks, n_tiles;
@@ -143,23 +161,73 @@ __device__ __forceinline__ void qkv_round32(const uint32_t (&a)[32], uint32_t (&
   for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
 }
 
-// RoPE on one row's features d0 .. d0+31 (x1, packed bf16) and d0+64 .. d0+95
-// (x2): x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin, every product and sum
-// rounded to fp32 separately, then to bf16.
-__device__ __forceinline__ void qkv_rotate32(uint32_t (&x1)[16], uint32_t (&x2)[16], const float* cs,
-                                             const float* sn) {
+// RoPE on one pair of features (x1: d, d+1 as packed bf16; x2: d+64, d+65):
+// x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin, every product and sum rounded
+// to fp32 separately, then to bf16.
+__device__ __forceinline__ void qkv_rotate2(uint32_t& x1, uint32_t& x2, float c0, float c1, float s0, float s1) {
+  const float a0 = bf16lo_to_f32(x1), a1 = bf16hi_to_f32(x1);
+  const float b0 = bf16lo_to_f32(x2), b1 = bf16hi_to_f32(x2);
+  const float y1a = __fadd_rn(__fmul_rn(a0, c0), -__fmul_rn(b0, s0));
+  const float y1b = __fadd_rn(__fmul_rn(a1, c1), -__fmul_rn(b1, s1));
+  const float y2a = __fadd_rn(__fmul_rn(b0, c0), __fmul_rn(a0, s0));
+  const float y2b = __fadd_rn(__fmul_rn(b1, c1), __fmul_rn(a1, s1));
+  x1 = pack_bf16x2(y1a, y1b);
+  x2 = pack_bf16x2(y2a, y2b);
+}
+
+// The warp's cos / sin staging (4 KB: cos [32 rows][16 features] then sin),
+// 16-byte piece q of row j at j * 64 + 16 (q ^ ((j >> 1) & 3)), so that the
+// stores (4 lanes per row) and the row reads (lane l: row l) hit distinct banks.
+__device__ __forceinline__ uint32_t qkv_tab_off(int j, int q) {
+  return uint32_t(j * 64 + ((q ^ ((j >> 1) & 3)) << 4));
+}
+
+// Coalesced loads of the warp's rows' table slice for features f0 .. f0+15
+// into v (cos in v[0..3], sin in v[4..7]): load k takes rows 8k .. 8k+7, four
+// lanes per row. trow / ok: this lane's table row and whether it is rotated.
+__device__ __forceinline__ void qkv_tab_load(const QkvParams& p, int trow, bool ok, int f0, int lane,
+                                             float4 (&v)[8]) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float a0 = bf16lo_to_f32(x1[e]), a1 = bf16hi_to_f32(x1[e]);
-    const float b0 = bf16lo_to_f32(x2[e]), b1 = bf16hi_to_f32(x2[e]);
-    const float c0 = cs[2 * e], c1 = cs[2 * e + 1], s0 = sn[2 * e], s1 = sn[2 * e + 1];
-    const float y1a = __fadd_rn(__fmul_rn(a0, c0), -__fmul_rn(b0, s0));
-    const float y1b = __fadd_rn(__fmul_rn(a1, c1), -__fmul_rn(b1, s1));
-    const float y2a = __fadd_rn(__fmul_rn(b0, c0), __fmul_rn(a0, s0));
-    const float y2b = __fadd_rn(__fmul_rn(b1, c1), __fmul_rn(a1, s1));
-    x1[e] = pack_bf16x2(y1a, y1b);
-    x2[e] = pack_bf16x2(y2a, y2b);
+  for (int k = 0; k < 4; ++k) {
+    const int j = 8 * k + (lane >> 2), q = lane & 3;
+    const int tr = __shfl_sync(0xffffffffu, trow, j);
+    const bool okj = __shfl_sync(0xffffffffu, ok ? 1 : 0, j) != 0;
+    const size_t off = (size_t)tr * 64 + f0 + q * 4;
+    v[k] = okj ? __ldg(reinterpret_cast<const float4*>(p.cos_tab + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[4 + k] = okj ? __ldg(reinterpret_cast<const float4*>(p.sin_tab + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+}
+
+__device__ __forceinline__ void qkv_tab_store(uint8_t* tab, int lane, const float4 (&v)[8]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 8 * k + (lane >> 2), q = lane & 3;
+    *reinterpret_cast<float4*>(tab + qkv_tab_off(j, q)) = v[k];
+    *reinterpret_cast<float4*>(tab + 2048 + qkv_tab_off(j, q)) = v[4 + k];
+  }
+}
+
+// RoPE on this lane's row for the 16 staged features (x1, packed bf16) and
+// their partners 64 further on (x2).
+__device__ __forceinline__ void qkv_rotate16_staged(uint32_t (&x1)[8], uint32_t (&x2)[8], const uint8_t* tab,
+                                                    int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 c4 = *reinterpret_cast<const float4*>(tab + qkv_tab_off(lane, q));
+    const float4 s4 = *reinterpret_cast<const float4*>(tab + 2048 + qkv_tab_off(lane, q));
+    qkv_rotate2(x1[2 * q], x2[2 * q], c4.x, c4.y, s4.x, s4.y);
+    qkv_rotate2(x1[2 * q + 1], x2[2 * q + 1], c4.z, c4.w, s4.z, s4.w);
+  }
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns into r[0..15].
+__device__ __forceinline__ void qkv_tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 template <bool kFused>
@@ -167,7 +235,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     qkv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const QkvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvStages * kQkvStageBytes);
+  QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvStages * kQkvStageBytes + (kFused ? kQkvTabBytes : 0));
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -178,7 +246,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->acc_full[s], 1);
-      mbar_init(&bars->acc_empty[s], 128);
+      mbar_init(&bars->acc_empty[s], kQkvEpiThreads);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -285,6 +353,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
+    const int part = (warp - 2) >> 2;  // 0: features 0..31 (+64) of each head, 1: 32..63 (+64)
     const int r = quad * 32 + lane;
     const uint32_t tlane = uint32_t(quad * 32) << 16;
     // The fused epilogue reads the cos / sin table of the kernel launched just
@@ -296,6 +365,36 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       qkv_tile(p, t, m, n);
       bool ok_all = true;
       for (int hf = 0; hf < 2; ++hf) {   // the tile's two 128-row halves, half 0 first
+      const int row = m * kQkvBM + hf * kQkvHM + r;
+      const bool live = row < p.M;
+      // Fused: the row's destinations, and the first table slice's loads, ahead
+      // of the accumulator wait (the warp is idle until then).
+      int b = 0, i = 0, s = 0, trow = 0;
+      bool write = false, kv_write = false;
+      size_t crow = 0;
+      const bool rotate = kFused && n < (kQHeads + kKVHeads) * kD / kQkvBN;  // query and key columns
+      float4 tv[8];
+      if (kFused) {
+        b = row / p.T;
+        i = row % p.T;
+        s = live ? __ldg(p.start_pos + b) : 0;
+        write = live && s >= 0 && (long long)s + p.T <= p.Tmax && (p.tab_n == 0 || (long long)s + p.T <= p.tab_n);
+        // with a position table no table kernel runs to report a bad start: the epilogue does
+        // (once, from the first column tile)
+        if (n == 0 && live && i == 0 && !write && p.tab_n > 0) report(p.status, GROK_DEV_BAD_START);
+        trow = write ? (p.tab_n > 0 ? s + i : row) : 0;  // table row of this token
+        // cache row of position s + i: contiguous b * Tmax + s + i; paged page * 128 + (s + i) % 128
+        crow = (size_t)b * p.Tmax + s + i;
+        kv_write = write;
+        if (p.pm.table && write) {
+          const int pos = s + i;
+          const int pg = __ldg(p.pm.table + (size_t)b * p.pm.max_pages + pos / GROK_PAGE_TOKENS);
+          kv_write = pg >= 0 && pg < p.pm.n_pages;
+          if (!kv_write) report(p.status, GROK_DEV_BAD_PAGE);
+          crow = (size_t)(kv_write ? pg : 0) * GROK_PAGE_TOKENS + pos % GROK_PAGE_TOKENS;
+        }
+        if (rotate) qkv_tab_load(p, trow, write, 32 * part, lane, tv);
+      }
       const bool ok = mbar_wait(&bars->acc_full[hf], tc & 1, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok_all = false;
@@ -303,12 +402,10 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       }
       tc_fence_after();
       const uint32_t acc = tmem + tlane + hf * kQkvBN;
-      const int row = m * kQkvBM + hf * kQkvHM + r;
-      const bool live = row < p.M;
       if (!kFused) {
         uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * p.N + n * kQkvBN) * 2;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * part; c < 4 * part + 4; ++c) {
           uint32_t a[32], o[16];
           tmem_ld32(acc + c * 32, a);
           tmem_wait_ld_dep(a);
@@ -319,66 +416,45 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           }
         }
       } else {
-        const int b = row / p.T, i = row % p.T;
-        const int s = live ? __ldg(p.start_pos + b) : 0;
-        const bool write = live && s >= 0 && (long long)s + p.T <= p.Tmax &&
-                           (p.tab_n == 0 || (long long)s + p.T <= p.tab_n);
-        // with a position table no table kernel runs to report a bad start: the epilogue does
-        if (live && i == 0 && !write && p.tab_n > 0) report(p.status, GROK_DEV_BAD_START);
-        const size_t trow = p.tab_n > 0 ? (size_t)(s + i) : (size_t)row;  // table row of this token
-        // cache row of position s + i: contiguous b * Tmax + s + i; paged page * 128 + (s + i) % 128
-        size_t crow = (size_t)b * p.Tmax + s + i;
-        bool kv_write = write;
-        if (p.pm.table && write) {
-          const int pos = s + i;
-          const int pg = __ldg(p.pm.table + (size_t)b * p.pm.max_pages + pos / GROK_PAGE_TOKENS);
-          kv_write = pg >= 0 && pg < p.pm.n_pages;
-          if (!kv_write) report(p.status, GROK_DEV_BAD_PAGE);
-          crow = (size_t)(kv_write ? pg : 0) * GROK_PAGE_TOKENS + pos % GROK_PAGE_TOKENS;
-        }
-        const bool rotate = n < (kQHeads + kKVHeads) * kD / kQkvBN;     // query and key columns
+        uint8_t* tab = smem + kQkvStages * kQkvStageBytes + (warp - 2) * kQkvTabWarpBytes;
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {   // the tile's two heads
-          const int col = n * kQkvBN + hh * kD;   // first output column of the head
-          uint8_t* dst;
-          const bool store = col < kQHeads * kD ? write : kv_write;
-          if (col < kQHeads * kD) {
-            dst = reinterpret_cast<uint8_t*>(p.q_rot) + ((size_t)row * kQHeads * kD + col) * 2;
-          } else if (col < (kQHeads + kKVHeads) * kD) {
-            const int g = (col - kQHeads * kD) / kD;
-            dst = reinterpret_cast<uint8_t*>(p.cache_k) + ((crow * kKVHeads + g) * kD) * 2;
-          } else {
-            const int g = (col - (kQHeads + kKVHeads) * kD) / kD;
-            dst = reinterpret_cast<uint8_t*>(p.cache_v) + ((crow * kKVHeads + g) * kD) * 2;
+        for (int pc = 0; pc < 2; ++pc) {   // features f0 .. f0+15 paired with 64+f0 ..
+          const int f0 = 32 * part + 16 * pc;
+          if (rotate) {
+            qkv_tab_store(tab, lane, tv);
+            __syncwarp();
+            if (pc == 0) qkv_tab_load(p, trow, write, f0 + 16, lane, tv);  // the next slice, while this one is used
           }
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {   // features 32c .. 32c+31 paired with 64+32c ..
-            uint32_t a[32], x1[16], x2[16];
-            tmem_ld32(acc + hh * kD + c * 32, a);
-            tmem_wait_ld_dep(a);
-            qkv_round32(a, x1);
-            tmem_ld32(acc + hh * kD + 64 + c * 32, a);
-            tmem_wait_ld_dep(a);
-            qkv_round32(a, x2);
-            if (rotate && write) {
-              float cs[32], sn[32];
-              const float4* cp = reinterpret_cast<const float4*>(p.cos_tab + trow * 64 + c * 32);
-              const float4* sp = reinterpret_cast<const float4*>(p.sin_tab + trow * 64 + c * 32);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 cv = __ldg(cp + q), sv = __ldg(sp + q);
-                cs[4 * q] = cv.x, cs[4 * q + 1] = cv.y, cs[4 * q + 2] = cv.z, cs[4 * q + 3] = cv.w;
-                sn[4 * q] = sv.x, sn[4 * q + 1] = sv.y, sn[4 * q + 2] = sv.z, sn[4 * q + 3] = sv.w;
-              }
-              qkv_rotate32(x1, x2, cs, sn);
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {   // the tile's two heads share the slice
+            const int col = n * kQkvBN + hh * kD;   // first output column of the head
+            uint8_t* dst;
+            const bool store = col < kQHeads * kD ? write : kv_write;
+            if (col < kQHeads * kD) {
+              dst = reinterpret_cast<uint8_t*>(p.q_rot) + ((size_t)row * kQHeads * kD + col) * 2;
+            } else if (col < (kQHeads + kKVHeads) * kD) {
+              const int g = (col - kQHeads * kD) / kD;
+              dst = reinterpret_cast<uint8_t*>(p.cache_k) + ((crow * kKVHeads + g) * kD) * 2;
+            } else {
+              const int g = (col - (kQHeads + kKVHeads) * kD) / kD;
+              dst = reinterpret_cast<uint8_t*>(p.cache_v) + ((crow * kKVHeads + g) * kD) * 2;
             }
+            uint32_t a[32], x1[8], x2[8];
+            qkv_tmem_ld16(acc + hh * kD + f0, a);
+            qkv_tmem_ld16(acc + hh * kD + 64 + f0, a + 16);
+            tmem_wait_ld_dep(a);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              x1[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+              x2[e] = pack_bf16x2(__uint_as_float(a[16 + 2 * e]), __uint_as_float(a[16 + 2 * e + 1]));
+            }
+            if (rotate && write) qkv_rotate16_staged(x1, x2, tab, lane);
             if (store) {
-              st_global_v8(dst + c * 64, x1);
-              st_global_v8(dst + c * 64 + 32, x1 + 8);
-              st_global_v8(dst + 128 + c * 64, x2);
-              st_global_v8(dst + 128 + c * 64 + 32, x2 + 8);
+              st_global_v8(dst + f0 * 2, x1);
+              st_global_v8(dst + 128 + f0 * 2, x2);
             }
           }
+          if (rotate) __syncwarp();  // every lane's reads of the slice before it is overwritten
         }
       }
       tc_fence_before();
@@ -481,14 +557,14 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   int dev = 0;
   if ((st = device_index(&dev)) != GROK_OK) return st;
   if (!attr_set[dev][fused]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, qkv_smem(fused));
     if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev][fused] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kQkvThreads);
-  cfg.dynamicSmemBytes = kQkvSmem;
+  cfg.dynamicSmemBytes = qkv_smem(fused);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the table kernel before it

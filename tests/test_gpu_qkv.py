@@ -109,6 +109,34 @@ def test_fused_from_position_table_equals_fused(small):
     assert torch.equal(ck3[1].view(torch.int16), ck2[1].view(torch.int16))   # sequence 1 (start 37) written
 
 
+def test_table_bad_start_in_the_second_half_of_a_row_tile():
+    """The epilogue reports a start beyond the position table from the row of
+    position 0 of the sequence; with T = 128 sequence 1's first row is the
+    second 128-row half of the first 256-row tile."""
+    B, T, Tmax = 2, 128, 512
+    inp = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[0, 300], seed=54)
+    x, w, start = inp.x.cuda(), inp.w.cuda(), inp.start_pos.cuda()
+    ctab, stab = G.rope_cos_sin(0, 400)   # sequence 1 needs positions up to 427
+    ck, cv = inp.cache_k.cuda(), inp.cache_v.cuda()
+    q_rot = torch.zeros((B, T, 48, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.qkv_rope_append_table(x, w, start, ctab, stab, q_rot, ck, cv, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == G.DEV_BAD_START
+    assert np.array_equal(W.bits(ck.cpu())[1], W.bits(inp.cache_k)[1])
+    assert np.array_equal(W.bits(cv.cpu())[1], W.bits(inp.cache_v)[1])
+    assert not W.bits(q_rot.cpu())[1].any()
+    # sequence 0 as the per-call-table version writes it
+    ck1, cv1 = inp.cache_k.cuda(), inp.cache_v.cuda()
+    q1 = torch.zeros_like(q_rot)
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.qkv_rope_append(x[:1], w, start[:1], q1[:1], ck1[:1], cv1[:1], G.alloc_qkv_workspace(1, T), st1)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0
+    assert torch.equal(q_rot[0].view(torch.int16), q1[0].view(torch.int16))
+    assert torch.equal(ck[0].view(torch.int16), ck1[0].view(torch.int16))
+
+
 def test_fused_full_size_sampled_rows():
     B, T, Tmax = 1, 8192, 8192
     inp = W.projection(B=B, T=T, Tmax=Tmax, start_pos=[0], seed=51)
