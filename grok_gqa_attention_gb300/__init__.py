@@ -46,6 +46,7 @@ EXPORTS = (
     "grok_rope_cos_sin",
     "grok_attn_prefill",
     "grok_attn_prefill_workspace",
+    "grok_attn_prefill_workspace_min",
     "grok_attn_prefill_ws",
     "grok_attn_decode_workspace",
     "grok_attn_decode",
@@ -107,6 +108,8 @@ def load() -> ctypes.CDLL:
     lib.grok_attn_prefill.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
     lib.grok_attn_prefill_workspace.restype = I
     lib.grok_attn_prefill_workspace.argtypes = [I, I, ctypes.POINTER(S)]
+    lib.grok_attn_prefill_workspace_min.restype = I
+    lib.grok_attn_prefill_workspace_min.argtypes = [I, I, ctypes.POINTER(S)]
     lib.grok_attn_prefill_ws.restype = I
     lib.grok_attn_prefill_ws.argtypes = [P, P, P, P, P, I, I, I, P, P, S, I, P, P]
     lib.grok_attn_decode_workspace.restype = I
@@ -258,9 +261,16 @@ def prefill(q_rot, cache_k, cache_v, start_pos, valid_len, out, dev_status=None,
 
 
 def prefill_workspace(B: int, Tmax: int) -> int:
-    """Bytes of the workspace prefill_ws() needs (fp16 copy of V and per-sequence flags)."""
+    """Bytes of workspace for prefill_ws() on the current device, with room for the key-range split."""
     n = ctypes.c_size_t(0)
     _check(load().grok_attn_prefill_workspace(B, Tmax, ctypes.byref(n)))
+    return n.value
+
+
+def prefill_workspace_min(B: int, Tmax: int) -> int:
+    """Smallest workspace prefill_ws() accepts (fp16 copy of V and flags; calls then run unsplit)."""
+    n = ctypes.c_size_t(0)
+    _check(load().grok_attn_prefill_workspace_min(B, Tmax, ctypes.byref(n)))
     return n.value
 
 

@@ -65,6 +65,8 @@
 // reaches 65504 (or any non-finite sum) puts its item on a fallback list in the
 // workspace, and so does every item of a sequence whose V does not fit fp16.
 // The bf16 mode of this kernel then recomputes exactly the listed items.
+#include <algorithm>
+
 #include "common.cuh"
 #include "host.cuh"
 
@@ -80,6 +82,8 @@ constexpr int kTileBytes = 2 * kBox;        // one K or V tile: two 64-wide halv
 constexpr int kPfData = kQBytes + 2 * kPfStages * kTileBytes;
 constexpr int kPfSeqCache = 512;  // sequences whose start / valid length are staged in shared memory
 constexpr float kPfHeadroom = 8.0f;  // fp16 mode: log2 gap between a row's reference and its first-tile maximum
+constexpr int kPfMaxParts = 4;       // key-range split: most units one item's key tiles are shared among
+constexpr int kPfMinPartTiles = 8;   // key-range split: fewest key tiles per unit
 
 struct PfBars {
   uint64_t q_full, q_empty;
@@ -89,6 +93,10 @@ struct PfBars {
   uint64_t lsum_ready[2];  // both halves of a slot posted their partial row sums
   uint64_t epi_done[2];    // the slot's eight epilogue warps' output stores have read their staging
   uint64_t xbar[2][4];     // fp16 mode: [slot][quad] both warps of a quadrant posted their first-tile maxima
+  uint64_t split_in[2];    // key-range split: the slot's eight epilogue warps wrote their unit's part
+  uint64_t split_out[2];   // key-range split: the unit is counted (split_last is set)
+  int split_last[2];       // key-range split: this unit is its item's last to finish (it adds the parts)
+  int split_over[2];       // key-range split: some row of this unit reached fp16's range
   float xmax[2][4][2][32];   // [slot][quad][half][lane]
   float lsum[2][2][2][128];  // [item parity][slot][half][row]
   int seq_start[kPfSeqCache], seq_valid[kPfSeqCache], seq_vflag[kPfSeqCache];
@@ -111,13 +119,23 @@ struct PfParams {
   // bf16 mode over a list of items only (the fallback pass): item_list[0 .. *item_count)
   const int32_t* item_list;
   const int32_t* item_count;
+  int n_units;  // work units of this pass (items, or in the split pass units of items)
+  // key-range split pass (fp16 mode): items [item_base, item_base + n_units / n_parts),
+  // each shared among n_parts units (unit = (item - item_base) * n_parts + part)
+  int item_base, n_parts;
+  float4* part_o;     // [unit][slot][half][16 feature quads][128 rows]: the unit's unnormalised O
+  float2* part_lm;    // [unit][slot][128 rows]: (row sum, reference) of the unit
+  int32_t* part_cnt;  // [item - item_base][slot]: units finished; zero at the start of the call
 };
 
 struct PfItem {
+  int item;         // the item this unit computes (part of)
+  int part, parts;  // key-range split: this unit's part and the item's number of parts (1: whole item)
+  int j0;           // first key tile of the unit
   int b, qt, g, hp;
   int s, n;     // start position, valid length
   int kv_end;   // keys [0, kv_end) are visible to some row of the tile
-  int n_kv;     // key tiles to visit (0: skip the item)
+  int n_kv;     // key tiles to visit from j0 (0: skip the unit)
   int n_sub;    // 64-key halves of those tiles that hold a visible key
   int bad;      // GROK_DEV_* bits when the sequence's integers are invalid
   bool redirect;  // fp16 mode: the sequence's V does not fit fp16; the fallback pass computes the item
@@ -134,12 +152,18 @@ __device__ __forceinline__ int pf_item_index(const PfParams& p, int rd) {
     const int n = min(__ldg(p.item_count), p.fb_cap);
     return idx < n ? __ldg(p.item_list + idx) : -1;
   }
-  return idx < p.n_items ? int(idx) : -1;
+  return idx < p.n_units ? int(idx) : -1;
 }
 
-template <bool kF16>
-__device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars, int item) {
+// Decode work unit `unit`. Outside the split pass a unit is a whole item.
+template <bool kF16, bool kSplit>
+__device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars, int unit) {
   PfItem it;
+  const int item = kSplit ? p.item_base + unit / p.n_parts : unit;
+  it.item = item;
+  it.part = kSplit ? unit % p.n_parts : 0;
+  it.parts = 1;
+  it.j0 = 0;
   it.hp = item % 3;
   int rest = item / 3;
   it.g = rest % kKVHeads;
@@ -177,6 +201,21 @@ __device__ __forceinline__ PfItem pf_item(const PfParams& p, const PfBars* bars,
   it.kv_end = min(it.s + last_row, it.s + it.n);
   it.n_sub = (it.kv_end + 63) / 64;
   it.n_kv = (it.n_sub + 1) / 2;
+  if (kSplit) {
+    // part k of `parts` takes key tiles [k n_kv / parts, (k + 1) n_kv / parts),
+    // at least kPfMinPartTiles each
+    const int parts = max(1, min(p.n_parts, it.n_kv / kPfMinPartTiles));
+    it.parts = parts;
+    if (it.part >= parts) {
+      it.n_kv = 0;
+      it.n_sub = 0;
+      return it;
+    }
+    const int j0 = it.part * it.n_kv / parts, j1 = (it.part + 1) * it.n_kv / parts;
+    it.j0 = j0;
+    it.n_sub = min(2 * j1, it.n_sub) - 2 * j0;
+    it.n_kv = j1 - j0;
+  }
   return it;
 }
 
@@ -385,8 +424,104 @@ __device__ __forceinline__ float pf_rowmax_half(uint32_t trow, int half, int rel
   return mx;
 }
 
-// kF16: fp16 mode; kList: bf16 mode over the fallback list only.
-template <bool kF16, bool kList>
+// Split-pass epilogue of one epilogue warp (slot, half, quad) for a unit whose
+// item is shared among `parts` units: the unit's unnormalised O (the warp's 32
+// rows x 64 features) and, from half 0, the rows' sums and references go to
+// the workspace; one thread per slot then counts the unit, and the item's last
+// unit to finish adds every part in part order (so the result does not depend
+// on which unit finishes last) and stages the output rows. Returns 1 when this
+// warp staged output rows, 0 when it has none to write, -1 when a bounded wait
+// gave up. Out of line: its registers stay out of the softmax loop's.
+__device__ __noinline__ int pf_split_epilogue(const PfParams& p, PfBars* bars, volatile int* abort, int unit,
+                                              int item, int parts, int slot, int half, int quad, int lane,
+                                              uint32_t trow, float lt, float mref, bool over, uint8_t* stage,
+                                              uint32_t parity) {
+  const int r = quad * 32 + lane;
+  const size_t su = size_t(unit) * 2 + slot;
+  float4* po = p.part_o + (su * 2 + half) * (16 * kPfRows) + r;
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t ov[32];
+    tmem_ld32(trow + 128 + half * 64 + cc * 32, ov);
+    tmem_wait_ld_dep(ov);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      po[(cc * 8 + q) * kPfRows] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
+                                               __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+  }
+  if (half == 0) p.part_lm[su * kPfRows + r] = make_float2(lt, mref);
+  tc_fence_before();
+  mbar_arrive(&bars->o_empty[slot]);  // O is read: the next unit's products may overwrite it
+  __threadfence();                    // this thread's part is visible before the item's count moves
+  __syncwarp();
+  if (lane == 0) {
+    if (over) atomicOr(&bars->split_over[slot], 1);
+    mbar_arrive(&bars->split_in[slot]);
+  }
+  if (half == 0 && quad == 0 && lane == 0) {
+    // one thread per slot counts the unit once all eight warps wrote theirs
+    int last = 0;
+    if (mbar_wait(&bars->split_in[slot], parity, abort, p.status)) {
+      __threadfence();
+      last = atomicAdd(p.part_cnt + item * 2 + slot, 1) == parts - 1;
+      if (bars->split_over[slot]) pf_fallback(p, p.item_base + item);  // the fallback pass recomputes the item
+      bars->split_over[slot] = 0;
+    }
+    bars->split_last[slot] = last;
+    mbar_arrive(&bars->split_out[slot]);
+  }
+  if (!mbar_wait(&bars->split_out[slot], parity, abort, p.status)) return -1;
+  if (!bars->split_last[slot]) return 0;
+  __threadfence();
+  // Part k's weights are 2^(t - m_k) (m_k its reference); on the common
+  // reference mx they are scaled by 2^(m_k - mx) <= 1.
+  const size_t su0 = size_t(item) * p.n_parts * 2 + slot;  // part 0 of the item, this slot
+  float2 lm[kPfMaxParts];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kPfMaxParts; ++k)
+    if (k < parts) {
+      lm[k] = __ldcg(p.part_lm + (su0 + 2 * k) * kPfRows + r);
+      mx = fmaxf(mx, lm[k].y);
+    }
+  float fk[kPfMaxParts];
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPfMaxParts; ++k)
+    if (k < parts) {
+      fk[k] = ex2_approx(lm[k].y - mx);
+      lsum = fmaf(lm[k].x, fk[k], lsum);
+    }
+  const float inv_l = 1.0f / lsum;
+#pragma unroll 2
+  for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row's 64 output features (8 bf16)
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPfMaxParts; ++k)
+      if (k < parts) {
+        const float4* pk4 = p.part_o + ((su0 + 2 * k) * 2 + half) * (16 * kPfRows) + r;
+        const float4 v0 = __ldcg(pk4 + (2 * c) * kPfRows), v1 = __ldcg(pk4 + (2 * c + 1) * kPfRows);
+        acc[0] = fmaf(v0.x, fk[k], acc[0]);
+        acc[1] = fmaf(v0.y, fk[k], acc[1]);
+        acc[2] = fmaf(v0.z, fk[k], acc[2]);
+        acc[3] = fmaf(v0.w, fk[k], acc[3]);
+        acc[4] = fmaf(v1.x, fk[k], acc[4]);
+        acc[5] = fmaf(v1.y, fk[k], acc[5]);
+        acc[6] = fmaf(v1.z, fk[k], acc[6]);
+        acc[7] = fmaf(v1.w, fk[k], acc[7]);
+      }
+    *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+        make_uint4(pack_bf16x2(acc[0] * inv_l, acc[1] * inv_l), pack_bf16x2(acc[2] * inv_l, acc[3] * inv_l),
+                   pack_bf16x2(acc[4] * inv_l, acc[5] * inv_l), pack_bf16x2(acc[6] * inv_l, acc[7] * inv_l));
+  }
+  return 1;
+}
+
+// kF16: fp16 mode; kList: bf16 mode over the fallback list only; kSplit:
+// fp16 mode over units that share their items' key tiles (the split pass).
+template <bool kF16, bool kList, bool kSplit>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -423,6 +558,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&bars->lsum_ready[s], 256);
       mbar_init(&bars->epi_done[s], 8);
       for (int q = 0; q < 4; ++q) mbar_init(&bars->xbar[s][q], 64);
+      mbar_init(&bars->split_in[s], 8);
+      mbar_init(&bars->split_out[s], 1);
+      bars->split_over[s] = 0;
     }
     mbar_init(&bars->mma_done, 2);
     bars->abort = 0;
@@ -454,7 +592,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       int kv_it = 0, q_it = 0;
       for (int rd = 0, item; (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
-        const PfItem it = pf_item<kF16>(p, bars, item);
+        const PfItem it = pf_item<kF16, kSplit>(p, bars, item);
         if (it.n_kv == 0) continue;
         if (!mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort, p.status)) break;
         mbar_arrive_expect_tx(&bars->q_full, kQBytes);
@@ -473,7 +611,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             break;
           }
           int krow, kb;
-          kv_coord(p.pm, it.b, j * kPfKeys, krow, kb, p.status);  // a tile is one page when paged
+          kv_coord(p.pm, it.b, (it.j0 + j) * kPfKeys, krow, kb, p.status);  // a tile is one page when paged
           mbar_arrive_expect_tx(&bars->k_full[st], kTileBytes);
           tma_load_4d(sK + st * kTileBytes, &tm_k, &bars->k_full[st], 0, it.g, krow, kb);
           tma_load_4d(sK + st * kTileBytes + kBox, &tm_k, &bars->k_full[st], 64, it.g, krow, kb);
@@ -509,7 +647,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int pc0 = 0, pc1 = 0;  // P hand-overs consumed per half (p_full parity)
     bool ok = true;
     for (int rd = 0, item; ok && (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item<kF16>(p, bars, item);
+      const PfItem it = pf_item<kF16, kSplit>(p, bars, item);
       if (it.n_kv == 0) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->q_full, q_it & 1, abort, p.status))) break;
       {
@@ -593,16 +731,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // query row within the tile
     const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + slot * 256;
-    int tile_cnt = 0, item_it = 0, sub_cnt = 0, xch_cnt = 0;
+    int tile_cnt = 0, item_it = 0, sub_cnt = 0, xch_cnt = 0, split_cnt = 0;
     for (int rd = 0, item; (item = pf_item_index<kList>(p, rd)) >= 0; ++rd) {
-      const PfItem it = pf_item<kF16>(p, bars, item);
+      const PfItem it = pf_item<kF16, kSplit>(p, bars, item);
       if (it.n_kv == 0) {
-        if (it.bad && slot == 0 && half == 0 && r == 0) report(p.status, it.bad);
-        if (kF16 && it.redirect && slot == 0 && half == 0 && r == 0) pf_fallback(p, item);
+        if (it.part == 0 && slot == 0 && half == 0 && r == 0) {
+          if (it.bad) report(p.status, it.bad);
+          if (kF16 && it.redirect) pf_fallback(p, it.item);
+        }
         continue;
       }
       const int i = it.qt * kPfRows + r;
-      const int lim = min(it.s + i, it.s + it.n - 1);  // last visible key of this row
+      // last visible key of this row, counted from the unit's first key
+      const int lim = min(it.s + i, it.s + it.n - 1) - it.j0 * kPfKeys;
       float l0 = 0.f, l1 = 0.f;
       float mref = kT;  // bf16 mode: the fixed reference logit 30 (30 log2(e) in log2 units)
       bool ok = true;
@@ -620,7 +761,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // are warp-collective (.sync.aligned).
         const bool unmasked = __all_sync(0xffffffffu, rel >= 64 * half + 63);
         if (kF16 && j == 0) {
-          // fp16 mode: the row's reference from the item's first tile (both halves)
+          // fp16 mode: the row's reference from the unit's first tile (both halves)
           float mx = unmasked ? pf_rowmax_half<false>(trow, half, rel) : pf_rowmax_half<true>(trow, half, rel);
           if (it.n_sub >= 2) {
             bars->xmax[slot][quad][half][lane] = mx;
@@ -633,7 +774,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             mx = fmaxf(mx, bars->xmax[slot][quad][half ^ 1][lane]);
           }
-          mref = kT * tanh_approx(mx * kY) + kPfHeadroom;  // key 0 is visible: mx is finite
+          // Key 0 is visible to every row, so mx is finite, except in a split
+          // unit after an item's first: rows with no visible key in it (all
+          // their weights zero) keep a finite reference through the clamp.
+          mref = kT * tanh_approx((kSplit ? fmaxf(mx, -1.0e30f) : mx) * kY) + kPfHeadroom;
         }
         if (unmasked)
           pf_softmax_half<false, kF16>(trow, half, rel, mref, l0, l1);
@@ -643,7 +787,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           // Zero the V rows of the last tile that lie beyond every visible key.
           // Both slots do it (same zeros) before handing over their P, since
           // each slot's PV product may be issued first.
-          const int first_dead = it.kv_end - j * kPfKeys;
+          const int first_dead = it.kv_end - (it.j0 + j) * kPfKeys;
           if (r >= first_dead) {
             const int st = (tile_cnt + j) % kPfStages;
             uint4* v0 = reinterpret_cast<uint4*>(sV + st * kTileBytes + r * 128);
@@ -677,37 +821,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const float lt = bars->lsum[item_it & 1][slot][0][r] + bars->lsum[item_it & 1][slot][1][r];
-      // fp16 mode: a weight sum that reached fp16's range means some weight may
-      // have overflowed: the fallback pass recomputes the item (a half-0 warp
-      // of each quadrant reports; duplicates are harmless)
-      if (kF16 && half == 0 && __any_sync(0xffffffffu, !(lt < 65504.0f)) && lane == 0) pf_fallback(p, item);
-      const float inv_l = 1.0f / lt;
       const int h = it.g * kGroup + it.hp * 2 + slot;
       const int st_last = (tile_cnt - 1) % kPfStages;
       uint8_t* stage = (slot == 0 ? sK : sV) + st_last * kTileBytes + half * kBox;
+      bool store = true;  // this warp's output rows are staged
+      if (!kSplit || it.parts == 1) {
+        // fp16 mode: a weight sum that reached fp16's range means some weight may
+        // have overflowed: the fallback pass recomputes the item (a half-0 warp
+        // of each quadrant reports; duplicates are harmless)
+        if (kF16 && half == 0 && __any_sync(0xffffffffu, !(lt < 65504.0f)) && lane == 0) pf_fallback(p, it.item);
+        const float inv_l = 1.0f / lt;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t ov[32];
-        tmem_ld32(trow + 128 + half * 64 + cc * 32, ov);
-        tmem_wait_ld_dep(ov);
-        uint32_t pk[16];
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(trow + 128 + half * 64 + cc * 32, ov);
+          tmem_wait_ld_dep(ov);
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = cc * 4 + q;  // 16-byte chunk of the row's 128 bytes
-          *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const int c = cc * 4 + q;  // 16-byte chunk of the row's 128 bytes
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty[slot]);  // O is read: the next item's products may overwrite it
+      } else {
+        const int res =
+            pf_split_epilogue(p, bars, abort, item, it.item - p.item_base, it.parts, slot, half, quad, lane, trow, lt,
+                              mref, __any_sync(0xffffffffu, !(lt < 65504.0f)), stage, uint32_t(split_cnt & 1));
+        ++split_cnt;
+        if (!__all_sync(0xffffffffu, res >= 0)) break;
+        store = res > 0;
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_empty[slot]);  // O is read: the next item's products may overwrite it
-      fence_proxy_async_smem();
+      if (store) fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         const int row0 = it.qt * kPfRows + quad * 32;
-        if (row0 < p.T) {
+        if (store && row0 < p.T) {
           tma_store_4d(&tm_o, stage + quad * 32 * 128, half * 64, h, row0, it.b);
           bulk_commit_group();
           bulk_wait_read_all();
@@ -746,7 +900,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // fp16 pass then hands all of that sequence's items to the fallback pass.
 __global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict__ cache_v, const int32_t* start_pos,
                                                         int T, int Tmax, int vh_rows, int from_start,
-                                                        uint4* __restrict__ vh, int32_t* v_flags) {
+                                                        uint4* __restrict__ vh, int32_t* v_flags, int32_t* zero,
+                                                        int n_zero) {
+  // the key-range split's per-item counters start at zero
+  if (blockIdx.y == 0)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0;
   const int b = blockIdx.y;
   const int s = __ldg(start_pos + b);
   if (s < 0 || (long long)s + T > Tmax) return;  // the attention passes skip this sequence
@@ -789,6 +947,12 @@ struct PfExtra {
   int32_t* fb_list = nullptr;
   int fb_cap = 0;
   bool fallback = false;            // bf16 mode over the listed items only, launched as a dependent
+  int n_units = -1;                 // units of this pass (-1: every item, whole)
+  bool split = false;               // fp16 split pass: items [item_base, ...) shared among n_parts units each
+  int item_base = 0, n_parts = 1;
+  float4* part_o = nullptr;
+  float2* part_lm = nullptr;
+  int32_t* part_cnt = nullptr;
 };
 
 static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
@@ -836,14 +1000,22 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
   prm.fb_cap = ex.fb_cap;
   prm.item_list = ex.fallback ? ex.fb_list : nullptr;
   prm.item_count = ex.fallback ? ex.fb_count : nullptr;
+  prm.n_units = ex.n_units >= 0 ? ex.n_units : prm.n_items;
+  prm.item_base = ex.split ? ex.item_base : 0;
+  prm.n_parts = ex.split ? ex.n_parts : 1;
+  prm.part_o = ex.part_o;
+  prm.part_lm = ex.part_lm;
+  prm.part_cnt = ex.part_cnt;
 
-  static bool attr_set[kMaxDevices][3] = {};  // per device and kernel instance; idempotent
+  static bool attr_set[kMaxDevices][4] = {};  // per device and kernel instance; idempotent
   int dev = 0;
   grok_status dst = device_index(&dev);
   if (dst != GROK_OK) return dst;
-  const int mode = ex.f16 ? 1 : ex.fallback ? 2 : 0;
-  auto kernel = mode == 1 ? prefill_kernel<true, false> : mode == 2 ? prefill_kernel<false, true>
-                                                                    : prefill_kernel<false, false>;
+  const int mode = ex.split ? 3 : ex.f16 ? 1 : ex.fallback ? 2 : 0;
+  auto kernel = mode == 3   ? prefill_kernel<true, false, true>
+                : mode == 1 ? prefill_kernel<true, false, false>
+                : mode == 2 ? prefill_kernel<false, true, false>
+                            : prefill_kernel<false, false, false>;
   if (!attr_set[dev][mode]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -853,7 +1025,7 @@ static grok_status prefill_launch(const grok_bf16* q_rot, const grok_bf16* k_src
   // device), so it takes one CTA per SM; it is a programmatic dependent of the
   // fp16 pass, so its launch overlaps that pass's tail, and it waits for the
   // whole fp16 grid (griddepcontrol.wait) before reading the list.
-  const int grid = ex.fallback ? sms : (prm.n_items < sms ? prm.n_items : sms);
+  const int grid = ex.fallback ? sms : (prm.n_units < sms ? prm.n_units : sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPfThreads);
@@ -908,22 +1080,56 @@ extern "C" grok_status grok_attn_prefill_paged(const grok_bf16* q_rot, const gro
 // Prefill with fp16 softmax weights (grok_attn_prefill_ws). Workspace layout:
 //   int32 v_flags[B], fb_count, fb_list[fb_cap]  (padded to 256 bytes)
 //   fp16 V copy [B][round_up(Tmax, 128)][8][128]
+//   optional, for the key-range split (at most one unit per SM):
+//     int32 part_cnt[sms][2] (padded to 256 bytes), float2 part_lm[sms][2][128],
+//     float4 part_o[sms][2][2][16][128]
 static int ws_vh_rows(int Tmax) { return (Tmax + kPfKeys - 1) / kPfKeys * kPfKeys; }
+static int prefill_items(int B, int T) { return B * ((T + kPfRows - 1) / kPfRows) * kKVHeads * 3; }
+
+// The key-range split. With fewer than two work items per SM, the items left
+// for the ragged last round (all of them when there are fewer items than SMs)
+// would hold their SMs while the rest idle: 192 equal items of a chunk over a
+// long cache on 152 SMs keep 40 SMs for two items. Those items are instead
+// shared among P = min(4, SMs / items) units each, run by a second pass, and
+// combined by each item's last unit to finish (at most one unit per SM, so the
+// partial outputs take at most SMs x 130 KB). Only caches of 16 key tiles or
+// more qualify, since a unit holds at least 8 tiles.
+static bool split_allowed(int Tmax) { return (Tmax + kPfKeys - 1) / kPfKeys >= 2 * kPfMinPartTiles; }
+static size_t split_cnt_bytes(int sms) { return (size_t(sms) * 2 * sizeof(int32_t) + 255) & ~size_t(255); }
+static size_t split_lm_bytes(int sms) { return size_t(sms) * 2 * kPfRows * sizeof(float2); }
+static size_t split_area_bytes(int sms) {
+  return split_cnt_bytes(sms) + split_lm_bytes(sms) + size_t(sms) * 2 * 2 * 16 * kPfRows * sizeof(float4);
+}
 static int ws_fb_cap(int B, int Tmax) {
   // items of the largest call (T = Tmax); each may be listed by up to 8
-  // quadrant warps of the fp16 pass plus once for its sequence's V
+  // quadrant warps of the fp16 pass (split items: once per slot by each of up
+  // to 4 units) plus once for its sequence's V
   return 9 * ((Tmax + kPfRows - 1) / kPfRows) * B * kKVHeads * 3;
 }
 static size_t ws_header_bytes(int B, int Tmax) {
   return ((size_t(B) + 1 + size_t(ws_fb_cap(B, Tmax))) * sizeof(int32_t) + 255) & ~size_t(255);
 }
 
-extern "C" grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes) {
-  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace: null pointer");
+// The part every call needs: the header and the fp16 V copy.
+static size_t ws_base_bytes(int B, int Tmax) {
+  return ws_header_bytes(B, Tmax) + size_t(B) * ws_vh_rows(Tmax) * kKVHeads * kD * 2;
+}
+
+extern "C" grok_status grok_attn_prefill_workspace_min(int B, int Tmax, size_t* bytes) {
+  if (!bytes) return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace_min: null pointer");
   if (B < 1 || Tmax < 1 || Tmax > GROK_MAX_POSITION || (long long)B * ws_vh_rows(Tmax) > (1LL << 31))
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace: need B >= 1, 1 <= Tmax <= %d",
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_workspace_min: need B >= 1, 1 <= Tmax <= %d",
                 GROK_MAX_POSITION);
-  *bytes = ws_header_bytes(B, Tmax) + size_t(B) * ws_vh_rows(Tmax) * kKVHeads * kD * 2;
+  *bytes = ws_base_bytes(B, Tmax);
+  return GROK_OK;
+}
+
+extern "C" grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes) {
+  grok_status st = grok_attn_prefill_workspace_min(B, Tmax, bytes);
+  if (st != GROK_OK || !split_allowed(Tmax)) return st;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != GROK_OK) return st;
+  *bytes += split_area_bytes(sms);
   return GROK_OK;
 }
 
@@ -942,13 +1148,26 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
     return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
                 GROK_MAX_POSITION, B, T, Tmax);
   size_t need = 0;
-  grok_status st = grok_attn_prefill_workspace(B, Tmax, &need);
+  grok_status st = grok_attn_prefill_workspace_min(B, Tmax, &need);
   if (st != GROK_OK) return st;
   if (workspace_bytes < need)
     return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, need);
   int sms = 0;
   if ((st = device_sm_count(&sms)) != GROK_OK) return st;
+  // items [0, n_whole) run whole; the rest, if the split applies, n_parts units each
+  const int n_items = prefill_items(B, T);
+  int n_whole = n_items, n_parts = 1;
+  if (n_items < 2 * sms && split_allowed(Tmax) && workspace_bytes >= need + split_area_bytes(sms)) {
+    const int rest = n_items % sms;
+    const int parts = rest > 0 ? std::min(kPfMaxParts, sms / rest) : 1;
+    if (parts > 1) {
+      n_whole = n_items - rest;
+      n_parts = parts;
+    }
+  }
+  const int n_split = n_items - n_whole;
+  char* split_area = static_cast<char*>(workspace) + need;
   const int vh_rows = ws_vh_rows(Tmax);
   int32_t* v_flags = static_cast<int32_t*>(workspace);
   int32_t* fb_count = v_flags + B;
@@ -967,9 +1186,9 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
     const long long cap = ((long long)sms * 8 + B - 1) / B;  // about 8 blocks per SM in all
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
-    v_to_half_kernel<<<dim3(unsigned(bx), unsigned(B)), 256, 0, s>>>(reinterpret_cast<const uint4*>(cache_v),
-                                                                     start_pos, T, Tmax, vh_rows, reuse_v_half ? 1 : 0,
-                                                                     static_cast<uint4*>(vh), v_flags);
+    v_to_half_kernel<<<dim3(unsigned(bx), unsigned(B)), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(cache_v), start_pos, T, Tmax, vh_rows, reuse_v_half ? 1 : 0,
+        static_cast<uint4*>(vh), v_flags, reinterpret_cast<int32_t*>(split_area), 2 * n_split);
     if ((st = check_launch("v_to_half")) != GROK_OK) return st;
   }
   PfExtra ex;
@@ -980,9 +1199,26 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
   ex.fb_count = fb_count;
   ex.fb_list = fb_list;
   ex.fb_cap = ws_fb_cap(B, Tmax);
-  if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
-                           valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
-    return st;
+  if (n_whole > 0) {
+    ex.n_units = n_whole;
+    if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                             valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
+      return st;
+  }
+  if (n_split > 0) {
+    ex.split = true;
+    ex.item_base = n_whole;
+    ex.n_parts = n_parts;
+    ex.n_units = n_split * n_parts;
+    ex.part_cnt = reinterpret_cast<int32_t*>(split_area);
+    ex.part_lm = reinterpret_cast<float2*>(split_area + split_cnt_bytes(sms));
+    ex.part_o = reinterpret_cast<float4*>(split_area + split_cnt_bytes(sms) + split_lm_bytes(sms));
+    if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                             valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
+      return st;
+  }
+  ex.split = false;
+  ex.n_units = -1;
   ex.f16 = false;
   ex.fallback = true;
   return prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,

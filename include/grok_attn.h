@@ -19,7 +19,7 @@
  * Calls by group:
  *   attention core      grok_rope_kv_append, grok_rope_kv_append_table, grok_rope_cos_sin,
  *                       grok_attn_prefill,
- *                       grok_attn_prefill_workspace, grok_attn_prefill_ws,
+ *                       grok_attn_prefill_workspace(_min), grok_attn_prefill_ws,
  *                       grok_attn_decode_workspace, grok_attn_decode, grok_attn_combine,
  *                       grok_attn_decode_step_static, grok_attn_decode_step(_workspace)
  *   projections         grok_qkv_project, grok_linear, grok_dequant_int8,
@@ -193,9 +193,19 @@ grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k, 
  * pass with bf16 weights from the bf16 cache, so every finite input is
  * handled; results then equal grok_attn_prefill's for those items.
  *   workspace: caller-owned device memory, 256-byte aligned, of at least
- *   grok_attn_prefill_workspace(B, Tmax) bytes (B * round_up(Tmax, 128) * 2 KB
- *   for the V copy plus a header of about B * Tmax / 128 * 864 bytes). Calls
- *   that overlap on the GPU need separate workspaces.
+ *   grok_attn_prefill_workspace_min(B, Tmax) bytes (B * round_up(Tmax, 128) *
+ *   2 KB for the V copy plus a header of about B * Tmax / 128 * 864 bytes).
+ *   grok_attn_prefill_workspace(B, Tmax) adds, for the current device, room
+ *   for the key-range split (SM count x 130 KB, about 20 MB on 152 SMs; none
+ *   when Tmax < 1921): when a call has fewer than two work items (128 query
+ *   rows x 2 heads) per SM, the items left for the last round (all of them
+ *   when there are fewer items than SMs) have their key tiles shared among up
+ *   to 4 work units of at least 8 tiles each, run by a second pass; each
+ *   unit's unnormalised output (fp32) goes to the workspace and the item's
+ *   last unit to finish adds them in unit order and writes the output. The
+ *   bits then do not depend on scheduling, but differ from an unsplit call's
+ *   within the same tolerance. With less workspace than that the call runs
+ *   unsplit. Calls that overlap on the GPU need separate workspaces.
  *   reuse_v_half: 0 = convert rows [0, start_pos[b] + T) (the call is self-
  *   contained). 1 = convert only rows [start_pos[b], start_pos[b] + T): rows
  *   below start_pos[b] must already be in this workspace from earlier calls
@@ -205,6 +215,7 @@ grok_status grok_attn_prefill(const grok_bf16* q_rot, const grok_bf16* cache_k, 
  *   beyond fp16 stays on the bf16 path until a call with 0.
  */
 grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* bytes);
+grok_status grok_attn_prefill_workspace_min(int B, int Tmax, size_t* bytes);
 grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k, const grok_bf16* cache_v,
                                  const int32_t* start_pos, const int32_t* valid_len, int B, int T, int Tmax,
                                  grok_bf16* out, void* workspace, size_t workspace_bytes, int reuse_v_half,

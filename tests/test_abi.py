@@ -55,6 +55,16 @@ def test_workspace_size_is_host_only(lib):
     assert lib.grok_attn_decode_workspace(1, 70000, ctypes.byref(n), ctypes.byref(s)) == 1
 
 
+def test_prefill_minimum_workspace_is_host_only(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.grok_attn_prefill_workspace_min(1, 8192, ctypes.byref(n)) == 0
+    v_half = 8192 * 8 * 128 * 2                      # fp16 copy of V
+    flags = (1 + 1 + 9 * 64 * 8 * 3) * 4             # v_flags, list count, fallback list
+    assert n.value == ((flags + 255) // 256) * 256 + v_half
+    assert lib.grok_attn_prefill_workspace_min(0, 8192, ctypes.byref(n)) == 1
+    assert lib.grok_attn_prefill_workspace_min(1, 70000, ctypes.byref(n)) == 1
+
+
 def test_null_pointers_rejected_before_any_device_call(lib):
     N = None
     assert lib.grok_rope_kv_append(N, N, N, N, 1, 1, 1, N, N, N, N, N) == 1

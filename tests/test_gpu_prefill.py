@@ -253,3 +253,65 @@ def test_prefill_ws_reusing_the_fp16_copy_across_chunks():
     ref = A.attention(W.bits(q_rot.cpu()), W.bits(ck.cpu()), W.bits(cv.cpu()), second.start_pos.numpy(),
                       second.valid_len.numpy())
     assert_close(W.bits(out.cpu()), ref, "second chunk, reused fp16 V")
+
+
+def _append_then_prefill_ws(inp, ws_bytes, dev="cuda", calls=1):
+    """Append, then grok_attn_prefill_ws `calls` times with a workspace of ws_bytes; output bits of each call."""
+    import grok_gqa_attention_gb300 as G
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    start = inp.start_pos.to(dev)
+    valid = None if inp.valid_len is None else inp.valid_len.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    q_rot = torch.empty_like(q)
+    G.rope_kv_append(q, k, v, start, q_rot, ck, cv, status)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(calls):
+        out = torch.empty_like(q_rot)
+        G.prefill_ws(q_rot, ck, cv, start, valid, out, ws, status)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return [W.bits(o.cpu()) for o in outs], (W.bits(q_rot.cpu()), W.bits(ck.cpu()), W.bits(cv.cpu()))
+
+
+def test_prefill_ws_key_split_matches_oracle():
+    """Two 128-token chunks over long caches give 48 work items, fewer than the GPU's
+    SMs, so grok_attn_prefill_ws runs them all in its split pass: sequence 1's items (25
+    key tiles) are shared among three units each, whose partial outputs the item's last
+    unit to finish adds; sequence 0's items (13 tiles, too few for two units of 8) run
+    whole. The result must match the oracle, be the same bits on a second call
+    (whichever unit finishes last), and differ from the unsplit call (a workspace of
+    grok_attn_prefill_workspace_min bytes; other references, other fp16 roundings) while
+    both stay within the tolerance."""
+    import grok_gqa_attention_gb300 as G
+    B, Tmax = 2, 4096
+    inp = W.custom(B=B, T=128, Tmax=Tmax, start_pos=[1500, 3000], valid_len=[128, 77], seed=41)
+    assert G.prefill_workspace(B, Tmax) > G.prefill_workspace_min(B, Tmax)
+    (split, split2), (rq, rk, rv) = _append_then_prefill_ws(inp, G.prefill_workspace(B, Tmax), calls=2)
+    (whole,), _ = _append_then_prefill_ws(inp, G.prefill_workspace_min(B, Tmax))
+    assert np.array_equal(split, split2)
+    assert not np.array_equal(split, whole)
+    ref = A.attention(rq, rk, rv, inp.start_pos.numpy(), inp.valid_len.numpy())
+    assert_close(split, ref, "key-range split")
+    assert_close(whole, ref, "unsplit")
+
+
+def test_prefill_ws_key_split_hands_overflowing_items_to_the_bf16_pass():
+    """With the split active (24 items, each shared among three units over 25 key tiles),
+    the first unit of every item sees a first tile of tiny logits and then saturated
+    ones: its weights would overflow fp16, so every item goes to the bf16 pass, whose
+    output equals grok_attn_prefill's bit for bit."""
+    import grok_gqa_attention_gb300 as G
+    Tmax = 4096
+    inp = W.custom(B=1, T=128, Tmax=Tmax, start_pos=[3072], seed=42, scale=3.0)
+    ck = inp.cache_k.float()
+    ck[:, :128] *= 0.02
+    ck[:, 128:3072] *= 4.0
+    inp.cache_k.copy_(ck.to(torch.bfloat16))
+    inp.k.copy_((inp.k.float() * 4.0).to(torch.bfloat16))
+    (out16,), _ = _append_then_prefill_ws(inp, G.prefill_workspace(1, Tmax))
+    _, _, _, outb, stb = run_prefill(inp, impl="bf16p")
+    assert stb == 0
+    assert np.array_equal(out16, outb)
