@@ -646,8 +646,26 @@ def run_paged(args, rank, dev):
     mc = float(np.median([a.elapsed_time(b_) for a, b_ in ev_c]))
     mp = float(np.median([a.elapsed_time(b_) for a, b_ in ev_p]))
     res["prefill"] = {"workload": PREFILL_WORKLOAD, "pages": n_pages, "ms_contiguous": mc, "ms_paged": mp,
-                      "paged_over_contiguous": mp / mc, "bit_identical": same}
-    del q_rot, ck, cv, kp, vp, out_c, out_p
+                      "paged_over_contiguous": mp / mc, "bit_identical": same, "calls": "grok_attn_prefill(_paged)"}
+    # the fp16-weight calls (the bench step's prefill) on the same pages
+    ws_c, ws_p = G.alloc_prefill_workspace(B, Tmax, dev), G.alloc_prefill_workspace(B, Tmax, dev)
+    for _ in range(2):
+        G.prefill_ws(q_rot, ck, cv, start, valid, out_c, ws_c, status)
+        G.prefill_ws_paged(q_rot, kp, vp, tab, start, valid, out_p, ws_p, status)
+    ev_c, ev_p = [], []
+    for _ in range(n):
+        ev_c.append(timed(lambda: G.prefill_ws(q_rot, ck, cv, start, valid, out_c, ws_c, status)))
+        ev_p.append(timed(lambda: G.prefill_ws_paged(q_rot, kp, vp, tab, start, valid, out_p, ws_p, status)))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the paged fp16 prefill")
+    same = bool(torch.equal(out_c.view(torch.int16), out_p.view(torch.int16)))
+    mc = float(np.median([a.elapsed_time(b_) for a, b_ in ev_c]))
+    mp = float(np.median([a.elapsed_time(b_) for a, b_ in ev_p]))
+    res["prefill_ws"] = {"workload": PREFILL_WORKLOAD, "pages": n_pages, "ms_contiguous": mc, "ms_paged": mp,
+                         "paged_over_contiguous": mp / mc, "bit_identical": same,
+                         "calls": "grok_attn_prefill_ws(_paged)"}
+    del q_rot, ck, cv, kp, vp, out_c, out_p, ws_c, ws_p
     torch.cuda.empty_cache()
 
     # decode
@@ -677,7 +695,8 @@ def run_paged(args, rank, dev):
     nbytes = decode_bytes((inp.start_pos + 1).numpy())
     res["decode"] = {"workload": DECODE_WORKLOAD, "pages": n_pages, "ms_contiguous": mc, "ms_paged": mp,
                      "paged_over_contiguous": mp / mc, "GB/s_paged": nbytes / (mp * 1e-3) / 1e9}
-    res["gpu_launches"] = 4 * n + 8
+    # prefill and decode: 2 kernels per pair of calls; the fp16 prefill: 3 per call (V copy, pass, fallback pass)
+    res["gpu_launches"] = 4 * n + 8 + 3 * (2 * n + 4)
     return res
 
 

@@ -67,6 +67,7 @@ EXPORTS = (
     "grok_linear_int8",
     "grok_rope_kv_append_paged",
     "grok_attn_prefill_paged",
+    "grok_attn_prefill_ws_paged",
     "grok_attn_decode_paged",
     "grok_qkv_rope_append_paged",
     "grok_kv_insert_slot",
@@ -150,6 +151,8 @@ def load() -> ctypes.CDLL:
     lib.grok_rope_kv_append_paged.argtypes = [P, P, P, P, I, I, P, P, P, I, P, I, P, P]
     lib.grok_attn_prefill_paged.restype = I
     lib.grok_attn_prefill_paged.argtypes = [P, P, P, I, P, I, P, P, I, I, P, P, P]
+    lib.grok_attn_prefill_ws_paged.restype = I
+    lib.grok_attn_prefill_ws_paged.argtypes = [P, P, P, I, P, I, P, P, I, I, P, P, S, I, P, P]
     lib.grok_attn_decode_paged.restype = I
     lib.grok_attn_decode_paged.argtypes = [P, P, P, I, P, I, P, I, P, S, P, P]
     lib.grok_qkv_rope_append_paged.restype = I
@@ -562,6 +565,25 @@ def prefill_paged(q_rot, k_pool, v_pool, block_table, start_pos, valid_len, out,
     _check(load().grok_attn_prefill_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table),
                                           max_pages, _ptr(start_pos), _ptr(valid_len), B, T, _ptr(out),
                                           _ptr(dev_status), _stream(stream)))
+
+
+def prefill_ws_paged(q_rot, k_pool, v_pool, block_table, start_pos, valid_len, out, workspace, dev_status=None,
+                     stream=None, reuse_v_half: bool = False) -> None:
+    """prefill_ws() over a paged cache; workspace sized by prefill_workspace(B, block_table.shape[1] * PAGE_TOKENS)."""
+    B, T = q_rot.shape[0], q_rot.shape[1]
+    _want(q_rot, "q_rot", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    n_pages, max_pages = _want_pages(k_pool, v_pool, block_table, B)
+    _want(start_pos, "start_pos", torch.int32, (B,))
+    if valid_len is not None:
+        _want(valid_len, "valid_len", torch.int32, (B,))
+    _want(out, "out", torch.bfloat16, (B, T, N_Q_HEADS, HEAD_DIM))
+    _want(workspace, "workspace", torch.uint8, (workspace.numel(),))
+    if dev_status is not None:
+        _want(dev_status, "dev_status", torch.int32, (1,))
+    _check(load().grok_attn_prefill_ws_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), n_pages, _ptr(block_table),
+                                             max_pages, _ptr(start_pos), _ptr(valid_len), B, T, _ptr(out),
+                                             _ptr(workspace), workspace.numel(), 1 if reuse_v_half else 0,
+                                             _ptr(dev_status), _stream(stream)))
 
 
 def decode_paged(q_rot, k_pool, v_pool, block_table, kv_len, workspace, dev_status=None, stream=None) -> None:

@@ -619,9 +619,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ok = false;
             break;
           }
+          // fp16 mode reads V from the copy in the workspace, contiguous per
+          // sequence whether or not the cache is paged
+          const int vrow = kF16 ? (it.j0 + j) * kPfKeys : krow, vb = kF16 ? it.b : kb;
           mbar_arrive_expect_tx(&bars->v_full[st], kTileBytes);
-          tma_load_4d(sV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, it.g, krow, kb);
-          tma_load_4d(sV + st * kTileBytes + kBox, &tm_v, &bars->v_full[st], 64, it.g, krow, kb);
+          tma_load_4d(sV + st * kTileBytes, &tm_v, &bars->v_full[st], 0, it.g, vrow, vb);
+          tma_load_4d(sV + st * kTileBytes + kBox, &tm_v, &bars->v_full[st], 64, it.g, vrow, vb);
         }
         if (!ok) break;
       }
@@ -894,14 +897,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 // ----------------------------------------------------------------------------
 // fp16 mode pre-pass: the fp16 copy of V. For sequence b with a valid start s,
-// rows [0, s + T) of the cache are rounded to nearest fp16 and rows
-// [s + T, round_up(s + T, 128)) are zeroed, so every key tile the fp16 pass
-// reads is finite. A finite |v| >= 65520 (beyond fp16) sets v_flags[b]: the
-// fp16 pass then hands all of that sequence's items to the fallback pass.
-__global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict__ cache_v, const int32_t* start_pos,
-                                                        int T, int Tmax, int vh_rows, int from_start,
-                                                        uint4* __restrict__ vh, int32_t* v_flags, int32_t* zero,
-                                                        int n_zero) {
+// rows [0, s + T) of the cache (contiguous, or through the block table) are
+// rounded to nearest fp16 and rows [s + T, round_up(s + T, 128)) are zeroed, so
+// every key tile the fp16 pass reads is finite. A finite |v| >= 65520 (beyond
+// fp16) sets v_flags[b]: the fp16 pass then hands all of that sequence's items
+// to the fallback pass.
+__global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict__ cache_v, PageMap pm,
+                                                        const int32_t* start_pos, int T, int Tmax, int vh_rows,
+                                                        int from_start, uint4* __restrict__ vh, int32_t* v_flags,
+                                                        int32_t* zero, int n_zero, int32_t* status) {
   // the key-range split's per-item counters start at zero
   if (blockIdx.y == 0)
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0;
@@ -917,7 +921,10 @@ __global__ void __launch_bounds__(256) v_to_half_kernel(const uint4* __restrict_
     const int row = int(e / kChunks), ch = int(e % kChunks);
     uint4 out = make_uint4(0, 0, 0, 0);
     if (row < rows) {
-      const uint4 in = __ldg(cache_v + ((size_t)b * Tmax + row) * kChunks + ch);
+      int src_row, src_b;
+      kv_coord(pm, b, row, src_row, src_b, status);  // (row, b) contiguous, (page row, 0) paged
+      const size_t rows_per_seq = pm.table ? size_t(0) : size_t(Tmax);
+      const uint4 in = __ldg(cache_v + ((size_t)src_b * rows_per_seq + src_row) * kChunks + ch);
       const uint32_t w[4] = {in.x, in.y, in.z, in.w};
       uint32_t o[4];
 #pragma unroll
@@ -1133,25 +1140,19 @@ extern "C" grok_status grok_attn_prefill_workspace(int B, int Tmax, size_t* byte
   return GROK_OK;
 }
 
-extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k,
-                                            const grok_bf16* cache_v, const int32_t* start_pos,
-                                            const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
-                                            void* workspace, size_t workspace_bytes, int reuse_v_half,
-                                            int32_t* dev_status, void* stream) {
-  if (!q_rot || !cache_k || !cache_v || !start_pos || !out || !workspace)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: null pointer");
-  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: bf16 tensors must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace must be 256-byte aligned");
-  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
-                GROK_MAX_POSITION, B, T, Tmax);
+// The fp16-weight prefill over a contiguous cache or a paged pool (pm), its
+// arguments already checked: V pre-pass, whole items, the split pass, then the
+// bf16 fallback pass over the listed items.
+static grok_status prefill_ws_run(const grok_bf16* q_rot, const grok_bf16* k_src, const grok_bf16* v_src,
+                                  uint64_t kv_rows, uint64_t kv_seqs, PageMap pm, const int32_t* start_pos,
+                                  const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out, void* workspace,
+                                  size_t workspace_bytes, int reuse_v_half, int32_t* dev_status, void* stream,
+                                  const char* what) {
   size_t need = 0;
   grok_status st = grok_attn_prefill_workspace_min(B, Tmax, &need);
   if (st != GROK_OK) return st;
   if (workspace_bytes < need)
-    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace of %zu bytes is smaller than the %zu needed",
+    return fail(GROK_ERR_INVALID_ARG, "%s: workspace of %zu bytes is smaller than the %zu needed", what,
                 workspace_bytes, need);
   int sms = 0;
   if ((st = device_sm_count(&sms)) != GROK_OK) return st;
@@ -1187,8 +1188,8 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
     v_to_half_kernel<<<dim3(unsigned(bx), unsigned(B)), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(cache_v), start_pos, T, Tmax, vh_rows, reuse_v_half ? 1 : 0,
-        static_cast<uint4*>(vh), v_flags, reinterpret_cast<int32_t*>(split_area), 2 * n_split);
+        reinterpret_cast<const uint4*>(v_src), pm, start_pos, T, Tmax, vh_rows, reuse_v_half ? 1 : 0,
+        static_cast<uint4*>(vh), v_flags, reinterpret_cast<int32_t*>(split_area), 2 * n_split, dev_status);
     if ((st = check_launch("v_to_half")) != GROK_OK) return st;
   }
   PfExtra ex;
@@ -1201,7 +1202,7 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
   ex.fb_cap = ws_fb_cap(B, Tmax);
   if (n_whole > 0) {
     ex.n_units = n_whole;
-    if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+    if ((st = prefill_launch(q_rot, k_src, v_src, kv_rows, kv_seqs, pm, start_pos,
                              valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
       return st;
   }
@@ -1213,7 +1214,7 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
     ex.part_cnt = reinterpret_cast<int32_t*>(split_area);
     ex.part_lm = reinterpret_cast<float2*>(split_area + split_cnt_bytes(sms));
     ex.part_o = reinterpret_cast<float4*>(split_area + split_cnt_bytes(sms) + split_lm_bytes(sms));
-    if ((st = prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+    if ((st = prefill_launch(q_rot, k_src, v_src, kv_rows, kv_seqs, pm, start_pos,
                              valid_len, B, T, Tmax, out, dev_status, stream, ex)) != GROK_OK)
       return st;
   }
@@ -1221,6 +1222,50 @@ extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_b
   ex.n_units = -1;
   ex.f16 = false;
   ex.fallback = true;
-  return prefill_launch(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+  return prefill_launch(q_rot, k_src, v_src, kv_rows, kv_seqs, pm, start_pos,
                         valid_len, B, T, Tmax, out, dev_status, stream, ex);
+}
+
+
+extern "C" grok_status grok_attn_prefill_ws(const grok_bf16* q_rot, const grok_bf16* cache_k,
+                                            const grok_bf16* cache_v, const int32_t* start_pos,
+                                            const int32_t* valid_len, int B, int T, int Tmax, grok_bf16* out,
+                                            void* workspace, size_t workspace_bytes, int reuse_v_half,
+                                            int32_t* dev_status, void* stream) {
+  if (!q_rot || !cache_k || !cache_v || !start_pos || !out || !workspace)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: null pointer");
+  if (!aligned16(q_rot) || !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: bf16 tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: workspace must be 256-byte aligned");
+  if (B < 1 || T < 1 || Tmax < 1 || T > Tmax || Tmax > GROK_MAX_POSITION)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws: need B >= 1, 1 <= T <= Tmax <= %d (B=%d T=%d Tmax=%d)",
+                GROK_MAX_POSITION, B, T, Tmax);
+  return prefill_ws_run(q_rot, cache_k, cache_v, uint64_t(Tmax), uint64_t(B), PageMap{nullptr, 0, 0}, start_pos,
+                        valid_len, B, T, Tmax, out, workspace, workspace_bytes, reuse_v_half, dev_status, stream,
+                        "grok_attn_prefill_ws");
+}
+
+extern "C" grok_status grok_attn_prefill_ws_paged(const grok_bf16* q_rot, const grok_bf16* k_pool,
+                                                  const grok_bf16* v_pool, int n_pages, const int32_t* block_table,
+                                                  int max_pages, const int32_t* start_pos, const int32_t* valid_len,
+                                                  int B, int T, grok_bf16* out, void* workspace,
+                                                  size_t workspace_bytes, int reuse_v_half, int32_t* dev_status,
+                                                  void* stream) {
+  if (!q_rot || !k_pool || !v_pool || !block_table || !start_pos || !out || !workspace)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws_paged: null pointer");
+  if (!aligned16(q_rot) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws_paged: bf16 tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(GROK_ERR_INVALID_ARG, "grok_attn_prefill_ws_paged: workspace must be 256-byte aligned");
+  const long long Tmax = (long long)max_pages * GROK_PAGE_TOKENS;
+  if (B < 1 || T < 1 || n_pages < 1 || max_pages < 1 || T > Tmax || Tmax > GROK_MAX_POSITION ||
+      (long long)n_pages * GROK_PAGE_TOKENS > (1LL << 31))
+    return fail(GROK_ERR_INVALID_ARG,
+                "grok_attn_prefill_ws_paged: need B, T, n_pages, max_pages >= 1, T <= max_pages * %d <= %d "
+                "(B=%d T=%d max_pages=%d n_pages=%d)",
+                GROK_PAGE_TOKENS, GROK_MAX_POSITION, B, T, max_pages, n_pages);
+  return prefill_ws_run(q_rot, k_pool, v_pool, uint64_t(n_pages) * GROK_PAGE_TOKENS, 1,
+                        PageMap{block_table, max_pages, n_pages}, start_pos, valid_len, B, T, int(Tmax), out,
+                        workspace, workspace_bytes, reuse_v_half, dev_status, stream, "grok_attn_prefill_ws_paged");
 }

@@ -26,7 +26,7 @@
  *                       grok_linear_int8(_workspace), grok_qkv_workspace, grok_qkv_rope_append,
  *                       grok_qkv_rope_append_table
  *   runtime             grok_prefill_pipe_create / _submit / _wait / _destroy
- *   paged cache         grok_rope_kv_append_paged, grok_attn_prefill_paged,
+ *   paged cache         grok_rope_kv_append_paged, grok_attn_prefill_paged, grok_attn_prefill_ws_paged,
  *                       grok_attn_decode_paged, grok_qkv_rope_append_paged
  *   continuous batching grok_kv_insert_slot
  *   diagnostics         grok_abi_version, grok_last_error, grok_selftest_bounded_wait
@@ -475,6 +475,12 @@ grok_status grok_prefill_pipe_destroy(grok_prefill_pipe* pipe);
  *   [start_pos[b], start_pos[b] + T) of sequence b through the table.
  * grok_attn_prefill_paged: grok_attn_prefill reading keys [0, start_pos[b] +
  *   valid_len[b]) of sequence b through the table.
+ * grok_attn_prefill_ws_paged: grok_attn_prefill_ws over the pools: K is read
+ *   through the table, and the call's fp16 copy of V (in the workspace, sized
+ *   by grok_attn_prefill_workspace(B, max_pages * GROK_PAGE_TOKENS)) is made
+ *   through the table, contiguous per sequence; reuse_v_half as for
+ *   grok_attn_prefill_ws. Bits equal grok_attn_prefill_ws over a contiguous
+ *   cache holding the same keys and values.
  * grok_attn_decode_paged: grok_attn_decode reading keys [0, kv_len[b]) through
  *   the table; workspace sized by grok_attn_decode_workspace(B, max_pages *
  *   GROK_PAGE_TOKENS) and combined with grok_attn_combine(..., Tmax = max_pages
@@ -495,6 +501,11 @@ grok_status grok_attn_prefill_paged(const grok_bf16* q_rot, const grok_bf16* k_p
                                     int n_pages, const int32_t* block_table, int max_pages,
                                     const int32_t* start_pos, const int32_t* valid_len, int B, int T,
                                     grok_bf16* out, int32_t* dev_status, void* stream);
+grok_status grok_attn_prefill_ws_paged(const grok_bf16* q_rot, const grok_bf16* k_pool, const grok_bf16* v_pool,
+                                       int n_pages, const int32_t* block_table, int max_pages,
+                                       const int32_t* start_pos, const int32_t* valid_len, int B, int T,
+                                       grok_bf16* out, void* workspace, size_t workspace_bytes, int reuse_v_half,
+                                       int32_t* dev_status, void* stream);
 grok_status grok_attn_decode_paged(const grok_bf16* q_rot, const grok_bf16* k_pool, const grok_bf16* v_pool,
                                    int n_pages, const int32_t* block_table, int max_pages, const int32_t* kv_len,
                                    int B, void* workspace, size_t workspace_bytes, int32_t* dev_status,

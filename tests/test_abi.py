@@ -97,6 +97,7 @@ def test_new_entry_points_reject_null_pointers_before_any_device_call(lib):
     # paged calls, slot insertion and the one-call decode step all check their pointers first
     assert lib.grok_attn_decode_paged(N, N, N, 1, N, 1, N, 1, N, 0, N, N) == 1
     assert lib.grok_attn_prefill_paged(N, N, N, 1, N, 1, N, N, 1, 1, N, N, N) == 1
+    assert lib.grok_attn_prefill_ws_paged(N, N, N, 1, N, 1, N, N, 1, 1, N, N, 0, 0, N, N) == 1
     assert lib.grok_rope_kv_append_paged(N, N, N, N, 1, 1, N, N, N, 1, N, 1, N, N) == 1
     assert lib.grok_kv_insert_slot(N, N, 1, 1, 0, N, N, 1, 1, N, 0, N) == 1
     assert lib.grok_attn_decode_step(N, N, N, N, 1, 1, N, N, N, 0, N, N, N) == 1

@@ -93,6 +93,71 @@ def test_paged_append_and_prefill_match_contiguous(case):
         assert_close(got, A.attention(rq, rk, rv, inp.start_pos.numpy(), vl), "paged prefill")
 
 
+WS_CASES = {
+    "chunks": PREFILL_CASES["chunks"],
+    # few items over long caches: the key-range split pass runs (48 items, 25-tile units)
+    "split": dict(B=2, T=128, Tmax=4096, start_pos=[1500, 3000], valid_len=[128, 77], seed=64),
+}
+
+
+@pytest.mark.parametrize("case", list(WS_CASES))
+def test_paged_fp16_prefill_matches_contiguous(case):
+    """grok_attn_prefill_ws_paged reads K through the table and makes its fp16 copy of V
+    through it: the bits equal grok_attn_prefill_ws over the contiguous caches, also when
+    the second call of a chunked prefill reuses the copy (reuse_v_half)."""
+    c = WS_CASES[case]
+    inp = W.custom(**c)
+    B, T, Tmax = c["B"], c["T"], c["Tmax"]
+    max_pages = Tmax // P
+    end = inp.start_pos.numpy() + T
+    table, n_pages, kp0, vp0 = _paged_setup(inp, max_pages, W.pages_needed(end), seed=c["seed"])
+    q_rot, ck, cv, st = run_append(inp, DEV)
+    assert st == 0
+    start = inp.start_pos.to(DEV)
+    valid = None if inp.valid_len is None else inp.valid_len.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = G.alloc_prefill_workspace(B, Tmax, DEV)
+    want = torch.empty_like(q_rot)
+    G.prefill_ws(q_rot, ck, cv, start, valid, want, ws, status)
+    q_rot_p, kp, vp, tab, st = _run_append_paged(inp, table, kp0, vp0)
+    assert st == 0
+    wsp = G.alloc_prefill_workspace(B, Tmax, DEV)
+    got = torch.empty_like(q_rot)
+    for reuse in (False, True):
+        got.zero_()
+        G.prefill_ws_paged(q_rot_p, kp, vp, tab, start, valid, got, wsp, status, reuse_v_half=reuse)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(W.bits(got.cpu()), W.bits(want.cpu())), f"reuse_v_half={reuse}"
+    rq, rk, rv = oracle_append(inp)
+    vl = None if inp.valid_len is None else inp.valid_len.numpy()
+    assert_close(W.bits(got.cpu()), A.attention(rq, rk, rv, inp.start_pos.numpy(), vl), f"paged fp16 prefill {case}")
+
+
+def test_paged_fp16_prefill_reports_a_bad_page():
+    """A table entry outside the pool sets GROK_DEV_BAD_PAGE (the V copy and the K loads read
+    page 0 in its place); the other sequence's rows keep the contiguous call's bits."""
+    c = WS_CASES["chunks"]
+    inp = W.custom(**c)
+    B, T, Tmax = c["B"], c["T"], c["Tmax"]
+    end = inp.start_pos.numpy() + T
+    table, n_pages, kp0, vp0 = _paged_setup(inp, Tmax // P, W.pages_needed(end), seed=c["seed"])
+    q_rot, ck, cv, st = run_append(inp, DEV)
+    start = inp.start_pos.to(DEV)
+    valid = inp.valid_len.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    want = torch.empty_like(q_rot)
+    G.prefill_ws(q_rot, ck, cv, start, valid, want, G.alloc_prefill_workspace(B, Tmax, DEV), status)
+    q_rot_p, kp, vp, tab, st = _run_append_paged(inp, table, kp0, vp0)
+    assert st == 0
+    tab[2, 0] = n_pages + 7   # sequence 2's first page id leaves the pool
+    got = torch.empty_like(q_rot)
+    G.prefill_ws_paged(q_rot_p, kp, vp, tab, start, valid, got, G.alloc_prefill_workspace(B, Tmax, DEV), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & G.DEV_BAD_PAGE
+    assert np.array_equal(W.bits(got[:2].cpu()), W.bits(want[:2].cpu()))
+
+
 def _decode(q_rot, ck, cv, kv_len, Tmax, table=None):
     B = q_rot.shape[0]
     ws = G.alloc_decode_workspace(B, Tmax, DEV)
