@@ -31,10 +31,14 @@
 //   warp 8     tcgen05.mma issuer (one lane) and TMEM owner: D[n, m] +=
 //              W^T[n, k] x^T[k, m] per 128-column half, M = 128 (n), N = 16 MT
 //              (m), K = 16, fp32 accumulators in TMEM (64 columns).
-// Then warps 0-7 read D (warp w: columns half w / 4, TMEM lanes 32 (w % 4)),
-// the 8 CTAs of a cluster add their partial sums through distributed shared
-// memory in a fixed rank order (so results do not depend on scheduling), and
-// CTA r rounds columns [32 r, 32 r + 32) to bf16 and writes them.
+// Then warps 0-7 read D (warp w: columns half w / 4, TMEM lanes 32 (w % 4),
+// i.e. columns [32 w, 32 w + 32) of the block). CTA r of the cluster finishes
+// columns [32 r, 32 r + 32): once every CTA's products are complete (a cluster
+// barrier; the A rings then serve as receive buffers), warp w of each CTA
+// stores its partial sums straight into CTA w's shared memory, in the slot of
+// its own rank, and after a second barrier each CTA adds the 8 slots in rank
+// order (so results do not depend on scheduling), rounds to bf16 and writes.
+// Remote stores need no round trip, unlike reading the other CTAs' partials.
 #include "common.cuh"
 #include "host.cuh"
 
@@ -57,7 +61,7 @@ constexpr int kI8XOff = kI8Stages * kI8WBytes;     // x ring after the weight ri
 constexpr int kI8AOff = kI8XOff + kI8XStages * kI8XBytes;
 constexpr int kI8Data = kI8AOff + kI8AStages * kI8ABytes;
 constexpr int kI8Smem = kI8Data + 256 + 1024;
-static_assert(32 * kI8Cols * 4 <= kI8AStages * kI8ABytes, "partial sums must fit in the A ring");
+static_assert(kI8Cluster * 32 * 32 * 4 <= kI8AStages * kI8ABytes, "received partial sums must fit in the A ring");
 
 struct I8Bars {
   uint64_t w_full[kI8Stages], w_empty[kI8Stages];
@@ -90,10 +94,8 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Four signed bytes -> four exact floats: byte b + 128 placed in the low
@@ -156,6 +158,8 @@ __global__ void __cluster_dims__(kI8Cluster, 1, 1) __launch_bounds__(kI8Threads,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  uint32_t d[32];     // converter warps: the accumulator's 32 columns of this warp
+  bool done = false;  // converter warps: every product completed (no wait gave up)
 
   if (warp == kI8DqWarps + 1) {
     // ------------------------------------------------------------ TMA producers
@@ -277,41 +281,38 @@ __global__ void __cluster_dims__(kI8Cluster, 1, 1) __launch_bounds__(kI8Threads,
         mbar_arrive(&bars->a_full[a]);
       }
     }
-    // D -> partial sums part[m][n] in the A ring (all products are complete)
-    const bool done = __all_sync(0xffffffffu, mbar_wait(&bars->d_full, 0, abort, status));
+    // D: this warp's 32 columns (32 warp + lane of the block), rows m < 16 MT
+    done = __all_sync(0xffffffffu, mbar_wait(&bars->d_full, 0, abort, status));
     tc_fence_after();
-    float* part = reinterpret_cast<float*>(sA);
-    const int nh = warp >> 2, quad = warp & 3;
-    uint32_t d[32];
-    tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + nh * 32, d);
+    tmem_ld32(tmem + (uint32_t((warp & 3) * 32) << 16) + (warp >> 2) * 32, d);
     tmem_wait_ld_dep(d);
-    if (done) {
-      const int n = nh * 128 + quad * 32 + lane;
-#pragma unroll
-      for (int m = 0; m < 16 * MT; ++m) part[m * kI8Cols + n] = __uint_as_float(d[m]);
-    }
   }
   tc_fence_before();
-  cluster_sync();  // every CTA's partial sums are in its shared memory
+  cluster_sync();  // every CTA's products are complete: its A ring may receive partial sums
+  if (warp < kI8DqWarps && done) {
+    // recv[src][m][c] (columns 32 w + c of the block) in CTA w = warp, slot src = this CTA
+    const uint32_t dst = dsmem_addr(smem_u32(sA) + uint32_t((rank * 32 * 32 + lane) * 4), uint32_t(warp));
+#pragma unroll
+    for (int m = 0; m < 16 * MT; ++m) st_dsmem_f32(dst + uint32_t(m * 32 * 4), __uint_as_float(d[m]));
+  }
+  cluster_sync();  // every partial sum has landed
   if (warp < kI8DqWarps) {
-    float* part = reinterpret_cast<float*>(sA);
+    const float* recv = reinterpret_cast<const float*>(sA);
     // CTA `rank` finishes columns [32 rank, 32 rank + 32): pairs of columns, rows < M
     for (int o = threadIdx.x; o < 16 * MT * 16; o += kI8DqWarps * 32) {
-      const int row = o / 16, col = 32 * rank + 2 * (o % 16);
+      const int row = o / 16, c = 2 * (o % 16);
       if (row < M) {
-        const uint32_t local = smem_u32(part + row * kI8Cols + col);
         float v0 = 0.f, v1 = 0.f;
 #pragma unroll
         for (int q = 0; q < kI8Cluster; ++q) {  // fixed order
-          const float2 v = ld_dsmem_f2(dsmem_addr(local, uint32_t(q)));
+          const float2 v = *reinterpret_cast<const float2*>(recv + (q * 32 + row) * 32 + c);
           v0 += v.x;
           v1 += v.y;
         }
-        y[(size_t(row) * N + n0 + col) / 2] = pack_bf16x2(v0, v1);
+        y[(size_t(row) * N + n0 + 32 * rank + c) / 2] = pack_bf16x2(v0, v1);
       }
     }
   }
-  cluster_sync();  // no CTA leaves while another reads its shared memory
   if (warp == kI8DqWarps) {
     tc_fence_after();
     tmem_dealloc(tmem, 64);
