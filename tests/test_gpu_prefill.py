@@ -315,3 +315,35 @@ def test_prefill_ws_key_split_hands_overflowing_items_to_the_bf16_pass():
     _, _, _, outb, stb = run_prefill(inp, impl="bf16p")
     assert stb == 0
     assert np.array_equal(out16, outb)
+
+
+def test_prefill_ws_key_split_skips_a_bad_sequence():
+    """The split pass with one sequence whose start leaves the cache: its units are skipped
+    (GROK_DEV_BAD_START, reported once), and the other sequence's split items still match
+    the oracle."""
+    import grok_gqa_attention_gb300 as G
+    B, Tmax = 2, 4096
+    good = W.custom(B=B, T=128, Tmax=Tmax, start_pos=[2000, 100], valid_len=[128, 128], seed=43)
+    q_rot, ck, cv, st = run_append_dev(good)
+    assert st == 0
+    start = torch.tensor([2000, Tmax - 64], dtype=torch.int32, device="cuda")  # sequence 1: start + T > Tmax
+    valid = good.valid_len.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q_rot)
+    G.prefill_ws(q_rot, ck, cv, start, valid, out, G.alloc_prefill_workspace(B, Tmax, "cuda"), status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == G.DEV_BAD_START
+    rq, rk, rv = W.bits(q_rot.cpu()), W.bits(ck.cpu()), W.bits(cv.cpu())
+    ref = A.attention(rq[:1], rk[:1], rv[:1], good.start_pos.numpy()[:1], good.valid_len.numpy()[:1])
+    assert_close(W.bits(out[:1].cpu()), ref, "split pass beside a bad sequence")
+
+
+def run_append_dev(inp, dev="cuda"):
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    q_rot = torch.empty_like(q)
+    import grok_gqa_attention_gb300 as G
+    G.rope_kv_append(q, k, v, inp.start_pos.to(dev), q_rot, ck, cv, status)
+    torch.cuda.synchronize()
+    return q_rot, ck, cv, int(status.item())
