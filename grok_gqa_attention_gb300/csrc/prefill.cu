@@ -65,6 +65,12 @@
 // reaches 65504 (or any non-finite sum) puts its item on a fallback list in the
 // workspace, and so does every item of a sequence whose V does not fit fp16.
 // The bf16 mode of this kernel then recomputes exactly the listed items.
+//
+// Split pass (kSplit, fp16 mode): when a call has fewer than two items per SM,
+// the items of the ragged last round run in a second launch, each shared among
+// up to four units over consecutive key tiles. A unit writes its unnormalised
+// O, row sums and references to the workspace; the item's last unit to finish
+// (a per-item counter) adds the parts in part order and writes the output.
 #include <algorithm>
 
 #include "common.cuh"
