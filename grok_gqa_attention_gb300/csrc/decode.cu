@@ -6,7 +6,7 @@
 // softmax, weighted sum of V); ch. 6 "model.py close reading II", §6.4.2.
 //
 // Memory-bound: one step streams K and V of every used cache row once
-// (512 bytes per row per KV head). Grid = (split, KV group, sequence); a CTA
+// (512 bytes per row per KV head). Grid = (KV group, sequence, split); a CTA
 // of 4 warps streams GROK_DECODE_SPLIT rows of one (sequence, group) through a
 // 3-stage TMA ring of 64-row tiles and keeps the group's 6 query heads as a
 // 16-row mma.sync operand (rows 6..15 zero): per 16 rows a warp computes
@@ -67,7 +67,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 
   // A dependent combine may be scheduled as soon as every CTA has started.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // split is the slowest grid dimension: the splits past a sequence's length, which
+  // leave at once, come after every split with work
+  const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long L_ = (long long)__ldg(kv_len + b) + kv_add;
   const int L = L_ < 1 || L_ > Tmax ? 0 : int(L_);
@@ -332,7 +334,7 @@ static grok_status decode_launch(const grok_bf16* q_rot, const grok_bf16* k_src,
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ns, kKVHeads, B);
+  cfg.gridDim = dim3(kKVHeads, B, ns);
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = kDecSmem;
   cfg.stream = static_cast<cudaStream_t>(stream);
