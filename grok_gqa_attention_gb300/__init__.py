@@ -485,7 +485,7 @@ def qkv_rope_append_table(x, w, start_pos, cos_tab, sin_tab, q_rot, cache_k, cac
 
 
 def linear(x, w, y, dev_status=None, stream=None) -> None:
-    """y [M, N] = x [M, K] . w [K, N] (bf16 Linear without bias; K % 64 == 0, N % 256 == 0)."""
+    """y [M, N] = x [M, K] . w [K, N] (bf16 Linear without bias; K % 64 == 0, N % 256 == 0 or N % 192 == 0)."""
     M, K = x.shape
     N = w.shape[1]
     _want(x, "x", torch.bfloat16, (M, K))

@@ -12,7 +12,7 @@
 // in TMEM, one rounding to bf16 per output. Output column h*128 + d is query
 // head h, 6144 + g*128 + d key head g, 7168 + g*128 + d value head g.
 // The same kernel with the plain epilogue is the general bias-free Linear
-// (grok_linear: any K that is a multiple of 64 and N of 256), which also
+// (grok_linear: any K that is a multiple of 64, N of 256 or of 192), which also
 // serves the output projection [M, 6144] . W_o [6144, 6144] and each
 // tensor-parallel rank's head slice of it.
 //
@@ -58,7 +58,7 @@ namespace grok {
 
 constexpr int kQkvK = 6144;                 // model size
 constexpr int kQkvN = 8192;                 // 48 * 128 + 2 * 8 * 128
-constexpr int kQkvBM = 256, kQkvBN = 256, kQkvBK = 64;  // tile: two 128-row MMA halves
+constexpr int kQkvBM = 256, kQkvBK = 64;  // tile: two 128-row MMA halves
 constexpr int kQkvHM = 128;                               // rows per MMA and per X box
 constexpr int kQkvStages = 3;
 constexpr int kQkvThreads = 320;
@@ -67,8 +67,14 @@ constexpr int kQkvGroupM = 16;  // 256-row blocks per tile group (8: 1 % slower,
 constexpr int kQkvABox = kQkvHM * kQkvBK * 2;               // 16 KB: one half's X block
 constexpr int kQkvABytes = 2 * kQkvABox;                    // 32 KB
 constexpr int kQkvBBox = kQkvBK * 64 * 2;                   // 8 KB: 64 K rows x 64 columns
-constexpr int kQkvBBytes = 4 * kQkvBBox;                    // 32 KB
-constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;     // 64 KB
+// The plain epilogue also runs with 192-column tiles (BN): for N = 6144 (the
+// output projection) 256-row x 256-column tiles leave a last round of 8 tiles
+// on 152 SMs (768 tiles, 0.84 of the rounds busy), 192-column ones fill 0.96
+// (1024 tiles).
+template <int BN>
+__host__ __device__ constexpr int qkv_stage_bytes() { return kQkvABytes + (BN / 64) * kQkvBBox; }   // 64 KB (256), 56 KB (192)
+// N the plain epilogue takes: whole 256- or 192-column tiles
+constexpr bool linear_n_ok(int N) { return N >= 192 && (N % 256 == 0 || N % 192 == 0); }
 
 struct QkvBars {
   uint64_t full[kQkvStages], empty[kQkvStages];
@@ -84,8 +90,8 @@ struct QkvBars {
 // slices (4 wavefronts), and the tile's two heads share them.
 constexpr int kQkvTabWarpBytes = 4096;
 constexpr int kQkvTabBytes = 8 * kQkvTabWarpBytes;
-constexpr int qkv_smem(bool fused) {
-  return kQkvStages * kQkvStageBytes + (fused ? kQkvTabBytes : 0) + int(sizeof(QkvBars)) + 1024;
+constexpr int qkv_smem(bool fused, int bn) {
+  return kQkvStages * (kQkvABytes + (bn / 64) * kQkvBBox) + (fused ? kQkvTabBytes : 0) + int(sizeof(QkvBars)) + 1024;
 }
 
 struct QkvParams {
@@ -230,12 +236,14 @@ __device__ __forceinline__ void qkv_tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
-template <bool kFused>
+template <bool kFused, int BN>
 __global__ void __launch_bounds__(kQkvThreads, 1)
     qkv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const QkvParams p) {
+  static_assert(BN == 256 || (!kFused && BN == 192), "tile width: two heads (fused), or 192 plain");
+  constexpr int kStageBytes = qkv_stage_bytes<BN>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvStages * kQkvStageBytes + (kFused ? kQkvTabBytes : 0));
+  QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvStages * kStageBytes + (kFused ? kQkvTabBytes : 0));
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -279,13 +287,13 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* sa = smem + st * kQkvStageBytes;
-          mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
+          uint8_t* sa = smem + st * kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
           tma_load_4d(sa, &tm_x, &bars->full[st], kb * kQkvBK, m * kQkvBM, 0, 0);
           tma_load_4d(sa + kQkvABox, &tm_x, &bars->full[st], kb * kQkvBK, m * kQkvBM + kQkvHM, 0, 0);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_load_4d(sa + kQkvABytes + c * kQkvBBox, &tm_w, &bars->full[st], n * kQkvBN + c * 64, kb * kQkvBK, 0, 0);
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_4d(sa + kQkvABytes + c * kQkvBBox, &tm_w, &bars->full[st], n * BN + c * 64, kb * kQkvBK, 0, 0);
         }
       }
       // Drain: copies still in flight (only after an abort) land before the CTA exits.
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = elect_one();
-    constexpr uint32_t idesc = make_idesc_bf16(kQkvHM, kQkvBN, 1);
+    constexpr uint32_t idesc = make_idesc_bf16(kQkvHM, BN, 1);
     int it = 0, tc = 0;
     bool ok = true;
     // TMEM: half 0 of the tile accumulates in columns 0..255, half 1 in 256..511.
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + st * kQkvStageBytes);
+        const uint32_t sa = smem_u32(smem + st * kStageBytes);
         const uint64_t bdesc = make_sdesc_sw128(sa + kQkvABytes, kQkvBBox, 1024);
         if (leader) {
           const uint64_t adesc = make_sdesc_sw128(sa, 16, 1024);
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           const uint64_t adesc = make_sdesc_sw128(sa + kQkvABox, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_ss(tmem + kQkvBN, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
+            umma_ss(tmem + BN, adesc + uint64_t((kk * 32) >> 4), bdesc + uint64_t((kk * 2048) >> 4), idesc,
                     (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars->empty[st]);
         }
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
       int b = 0, i = 0, s = 0, trow = 0;
       bool write = false, kv_write = false;
       size_t crow = 0;
-      const bool rotate = kFused && n < (kQHeads + kKVHeads) * kD / kQkvBN;  // query and key columns
+      const bool rotate = kFused && n < (kQHeads + kKVHeads) * kD / BN;  // query and key columns
       float4 tv[8];
       if (kFused) {
         b = row / p.T;
@@ -401,11 +409,12 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t acc = tmem + tlane + hf * kQkvBN;
+      const uint32_t acc = tmem + tlane + hf * BN;
       if (!kFused) {
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * p.N + n * kQkvBN) * 2;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.y) + ((size_t)row * p.N + n * BN) * 2;
+        constexpr int kChunks = BN / 64;  // 32-column chunks per part
 #pragma unroll
-        for (int c = 4 * part; c < 4 * part + 4; ++c) {
+        for (int c = kChunks * part; c < kChunks * part + kChunks; ++c) {
           uint32_t a[32], o[16];
           tmem_ld32(acc + c * 32, a);
           tmem_wait_ld_dep(a);
@@ -416,7 +425,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           }
         }
       } else {
-        uint8_t* tab = smem + kQkvStages * kQkvStageBytes + (warp - 2) * kQkvTabWarpBytes;
+        uint8_t* tab = smem + kQkvStages * kStageBytes + (warp - 2) * kQkvTabWarpBytes;
 #pragma unroll 1
         for (int pc = 0; pc < 2; ++pc) {   // features f0 .. f0+15 paired with 64+f0 ..
           const int f0 = 32 * part + 16 * pc;
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1)
           }
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {   // the tile's two heads share the slice
-            const int col = n * kQkvBN + hh * kD;   // first output column of the head
+            const int col = n * BN + hh * kD;   // first output column of the head
             uint8_t* dst;
             const bool store = col < kQHeads * kD ? write : kv_write;
             if (col < kQHeads * kD) {
@@ -548,23 +557,35 @@ grok_status qkv_launch(bool fused, const grok_bf16* x, const grok_bf16* w, int M
   prm.K = K;
   prm.N = N;
   prm.k_blocks = K / kQkvBK;
-  prm.n_ntiles = N / kQkvBN;
   prm.n_mtiles = (M + kQkvBM - 1) / kQkvBM;
+  // tile width: 256 columns (two heads; the fused epilogue needs it), or for the
+  // plain epilogue 192 when that keeps more of the rounds of tiles busy
+  int bn = 256;
+  if (!fused && N % 192 == 0) {
+    auto busy = [&](int w) {
+      const long long tiles = (long long)prm.n_mtiles * (N / w);
+      const long long rounds = (tiles + sms - 1) / sms;
+      return double(tiles) / double(rounds * sms);
+    };
+    if (N % 256 != 0 || busy(192) > busy(256) + 1e-9) bn = 192;
+  }
+  prm.n_ntiles = N / bn;
   prm.n_tiles = prm.n_mtiles * prm.n_ntiles;
   const int grid = prm.n_tiles < sms ? prm.n_tiles : sms;
-  auto kernel = fused ? qkv_kernel<true> : qkv_kernel<false>;
-  static bool attr_set[kMaxDevices][2] = {};  // per device and epilogue; idempotent
+  auto kernel = fused ? qkv_kernel<true, 256> : bn == 192 ? qkv_kernel<false, 192> : qkv_kernel<false, 256>;
+  const int kind = fused ? 1 : bn == 192 ? 2 : 0;
+  static bool attr_set[kMaxDevices][3] = {};  // per device and kernel instance; idempotent
   int dev = 0;
   if ((st = device_index(&dev)) != GROK_OK) return st;
-  if (!attr_set[dev][fused]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, qkv_smem(fused));
+  if (!attr_set[dev][kind]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, qkv_smem(fused, bn));
     if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    attr_set[dev][fused] = true;
+    attr_set[dev][kind] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kQkvThreads);
-  cfg.dynamicSmemBytes = qkv_smem(fused);
+  cfg.dynamicSmemBytes = qkv_smem(fused, bn);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the table kernel before it
@@ -585,10 +606,10 @@ extern "C" grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M
   if (!x || !w || !y) return fail(GROK_ERR_INVALID_ARG, "grok_linear: null pointer");
   if (!aligned16(x) || !aligned16(w) || !aligned32(y))
     return fail(GROK_ERR_INVALID_ARG, "grok_linear: x and w must be 16-byte aligned, y 32-byte aligned");
-  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || N < kQkvBN || N % kQkvBN != 0)
+  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || !linear_n_ok(N))
     return fail(GROK_ERR_INVALID_ARG,
-                "grok_linear: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)", kQkvBK,
-                kQkvBN, M, K, N);
+                "grok_linear: need 1 <= M <= 2^30, K a positive multiple of %d, N of 256 or of 192 (M=%d K=%d N=%d)",
+                kQkvBK, M, K, N);
   QkvParams prm = {};
   prm.T = 1;
   prm.Tmax = 1;
@@ -763,10 +784,11 @@ extern "C" grok_status grok_linear_int8(const grok_bf16* x, const int8_t* w8, co
     return fail(GROK_ERR_INVALID_ARG, "grok_linear_int8: workspace of %zu bytes, need %zu", ws_bytes,
                 size_t(K) * N * sizeof(grok_bf16));
   // grok_linear's shape rules first, so that nothing is queued for a call it would reject
-  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || N < kQkvBN || N % kQkvBN != 0)
+  if (M < 1 || M > (1 << 30) || K < kQkvBK || K % kQkvBK != 0 || !linear_n_ok(N))
     return fail(GROK_ERR_INVALID_ARG,
-                "grok_linear_int8: need 1 <= M <= 2^30, K a positive multiple of %d, N of %d (M=%d K=%d N=%d)",
-                kQkvBK, kQkvBN, M, K, N);
+                "grok_linear_int8: need 1 <= M <= 2^30, K a positive multiple of %d, N of 256 or of 192 (M=%d K=%d "
+                "N=%d)",
+                kQkvBK, M, K, N);
   // Decode-sized M: one pass over the int8 weight, dequantized in shared memory
   // (int8_small.cu).
   if (small_int8_ok(M, K, N)) {

@@ -355,7 +355,7 @@ grok_status grok_qkv_project(const grok_bf16* x, const grok_bf16* w, int M, grok
 /*
  * A bias-free Linear (ch. 4 §4.1) on the same tensor-core kernel:
  * y [M, N] = x [M, K] . w [K, N], bf16, fp32 accumulation, one rounding.
- * K must be a positive multiple of 64 and N of 256; 1 <= M <= 2^30. Row-major
+ * K must be a positive multiple of 64 and N of 256 or of 192; 1 <= M <= 2^30. Row-major
  * device tensors, x and w 16-byte aligned, y 32-byte aligned. Serves the output projection (ch. 4 §4.5.4:
  * attention output [B*T, 48*128] head-major . W_o [6144, 6144]) and each
  * tensor-parallel rank's share of it (the rows of W_o for the rank's heads,
@@ -375,7 +375,7 @@ grok_status grok_linear(const grok_bf16* x, const grok_bf16* w, int M, int K, in
  * grok_linear_int8: y [M, N] = x [M, K] . dequant(w8, scales): the weight is
  *   dequantized into the caller's workspace (at least
  *   grok_linear_int8_workspace(K, N) bytes, K*N bf16) and then multiplied by
- *   grok_linear (so K % 64 == 0, N % 256 == 0). For prefill-sized M the
+ *   grok_linear (so K % 64 == 0, N % 256 == 0 or N % 192 == 0). For prefill-sized M the
  *   product is tensor-bound and the one pass over the weight costs a few
  *   percent; the workspace may be reused across calls with the same weight.
  *   For decode-sized M (M <= 32, K a multiple of 512) the weight is instead

@@ -112,6 +112,14 @@ def test_misaligned_outputs_rejected_before_any_device_call(lib):
     assert lib.grok_dequant_int8(a32, a32, 64, 256, a16, None) == 1
 
 
+def test_linear_tile_widths_rejected_before_any_device_call(lib):
+    """N must fill whole 256- or 192-column tiles: 320, 128 and 64 do neither."""
+    a32 = ctypes.c_void_p(1 << 20)
+    for n in (320, 128, 64, 0):
+        assert lib.grok_linear(a32, a32, 256, 64, n, a32, None, None) == 1
+        assert b"N of 256 or of 192" in lib.grok_last_error()
+
+
 def test_product_path_has_no_cpu_route():
     """The binding computes nothing itself: CPU tensors are refused, a missing library
     raises, and no file of the package or its CUDA sources refers to the oracle."""

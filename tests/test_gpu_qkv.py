@@ -200,7 +200,10 @@ def _rand(gen, shape, scale):
     return (torch.randn(*shape, generator=gen) * scale).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 64, 256), (130, 128, 512), (257, 6144, 256), (64, 768, 6144)])
+# 192-column tiles: N = 576 and 192 are only multiples of 192; N = 6144 at M = 64
+# and 600 picks them too (more of the last round of tiles busy)
+@pytest.mark.parametrize("M,K,N", [(1, 64, 256), (130, 128, 512), (257, 6144, 256), (64, 768, 6144),
+                                   (600, 192, 6144), (300, 192, 576), (1, 64, 192)])
 def test_linear_shapes_match_oracle(M, K, N):
     gen = torch.Generator().manual_seed(M * 7 + K + N)
     x = _rand(gen, (M, K), 1.0)
