@@ -797,8 +797,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           // Both slots do it (same zeros) before handing over their P, since
           // each slot's PV product may be issued first.
           const int first_dead = it.kv_end - (it.j0 + j) * kPfKeys;
+          const int st = (tile_cnt + j) % kPfStages;
+          // The tile's V may still be landing: for a half-0 step the issuer has
+          // not waited for it yet, and the zeros must not be overwritten by it.
+          const bool vw = mbar_wait(&bars->v_full[st], ((tile_cnt + j) / kPfStages) & 1, abort, p.status);
+          if (!__all_sync(0xffffffffu, vw)) {
+            ok = false;
+            break;
+          }
           if (r >= first_dead) {
-            const int st = (tile_cnt + j) % kPfStages;
             uint4* v0 = reinterpret_cast<uint4*>(sV + st * kTileBytes + r * 128);
             uint4* v1 = reinterpret_cast<uint4*>(sV + st * kTileBytes + kBox + r * 128);
             const uint4 z = make_uint4(0, 0, 0, 0);
