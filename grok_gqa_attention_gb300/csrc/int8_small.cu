@@ -157,6 +157,11 @@ __global__ void __cluster_dims__(kI8Cluster, 1, 1) __launch_bounds__(kI8Threads,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Launched as a programmatic dependent: the setup above (and the CTA launch)
+  // overlaps the previous kernel's tail on the stream. Nothing in global memory
+  // is read or written before the wait, so stream order holds for every operand.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tmem = bars->tmem_base;
   uint32_t d[32];     // converter warps: the accumulator's 32 columns of this warp
   bool done = false;  // converter warps: every product completed (no wait gave up)
@@ -351,8 +356,19 @@ grok_status linear_int8_small(const grok_bf16* x, const int8_t* w8, const float*
     if (e != cudaSuccess) return fail(cuda_status(e), "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     attr_set[dev][mt - 1] = true;
   }
-  kernel<<<dim3(kI8Cluster, unsigned(N / kI8Cols)), kI8Threads, kI8Smem, static_cast<cudaStream_t>(stream)>>>(
-      tx, tw, scales, M, K, N, reinterpret_cast<uint32_t*>(y), dev_status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kI8Cluster, unsigned(N / kI8Cols));
+  cfg.blockDim = dim3(kI8Threads);
+  cfg.dynamicSmemBytes = kI8Smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's griddepcontrol.wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kernel, tx, tw, scales, M, K, N, reinterpret_cast<uint32_t*>(y), dev_status);
+  if (e != cudaSuccess) return fail(cuda_status(e), "linear_int8_small launch: %s", cudaGetErrorString(e));
   return check_launch("linear_int8_small");
 }
 
