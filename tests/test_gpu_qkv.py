@@ -270,9 +270,11 @@ def test_dequant_int8_bit_exact(K, N):
     assert np.array_equal(W.bits(w16.cpu()), P.dequant_int8(w8.numpy(), scales.numpy()))
 
 
-def test_linear_int8_matches_oracle():
-    gen = torch.Generator().manual_seed(70)
-    M, K, N = 130, 768, 512
+@pytest.mark.parametrize("M,K,N", [(130, 768, 512), (32, 512, 576)])
+def test_linear_int8_matches_oracle(M, K, N):
+    """Dequantize-then-multiply; N = 576 (a multiple of 192, not of 256) takes it at M = 32 too,
+    on 192-column tiles."""
+    gen = torch.Generator().manual_seed(70 + N)
     x = _rand(gen, (M, K), 1.0)
     w8, scales = _int8_weight(gen, K, N)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
