@@ -18,14 +18,15 @@
 //
 // Persistent kernel, one CTA per SM, 10 warps:
 //   warp 0      TMA producer: per 64-wide K block two X boxes [128 rows x 64]
-//               and four W boxes [64 rows x 64 columns] (64 KB) into a 3-stage
-//               ring
+//               and four W boxes [64 rows x 64 columns] (64 KB; three, 56 KB,
+//               with 192-column tiles) into a 3-stage ring
 //   warp 1      TMEM owner and MMA issuer (converged; one fixed lane issues)
 //   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
 //               row per thread; of the two warps on a lane quarter, warps 2-5
 //               take the first half of every head's features (fused: 0..31
 //               with their rotation partners 64..95), warps 6-9 the second
-// Tile = 256 rows x 256 columns (two heads), as two 128-row halves that share
+// Tile = 256 rows x 256 columns (two heads; the plain epilogue also runs 256 x
+// 192 tiles, see qkv_stage_bytes), as two 128-row halves that share
 // each staged W block: tcgen05.mma M=128, N=256, K=16 per half, A = X
 // (K-major), B = W (N-contiguous rows, MN-major), both 128-byte swizzled. The
 // halves accumulate in TMEM columns 0..255 and 256..511. Sharing W between the
