@@ -96,7 +96,8 @@ def source_digest(*paths: str) -> str:
 KERNEL_SOURCES = {
     "qkv_kernel": ("grok_gqa_attention_gb300/csrc/qkv.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
     "prefill_kernel": ("grok_gqa_attention_gb300/csrc/prefill.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
-    "decode_kernel": ("grok_gqa_attention_gb300/csrc/decode.cu", "grok_gqa_attention_gb300/csrc/common.cuh"),
+    "decode_kernel": ("grok_gqa_attention_gb300/csrc/decode.cu", "grok_gqa_attention_gb300/csrc/common.cuh",
+                      "include/grok_attn.h"),  # (the header fixes the split size)
 }
 
 

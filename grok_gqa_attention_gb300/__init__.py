@@ -17,7 +17,7 @@ import torch
 N_Q_HEADS = 48
 N_KV_HEADS = 8
 HEAD_DIM = 128
-DECODE_SPLIT = 512
+DECODE_SPLIT = 1024
 MAX_POSITION = 65536
 
 DEV_BAD_START = 0x1

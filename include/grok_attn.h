@@ -71,14 +71,15 @@
 extern "C" {
 #endif
 
-#define GROK_ATTN_ABI_VERSION 1
+/* 2: GROK_DECODE_SPLIT went from 512 to 1024 keys (decode workspace sizes changed) */
+#define GROK_ATTN_ABI_VERSION 2
 
 #define GROK_N_Q_HEADS 48
 #define GROK_N_KV_HEADS 8
 #define GROK_HEAD_DIM 128
 #define GROK_MAX_POSITION 65536
 /* keys per decode split (one partial result per split) */
-#define GROK_DECODE_SPLIT 512
+#define GROK_DECODE_SPLIT 1024
 
 typedef uint16_t grok_bf16;
 

@@ -40,16 +40,16 @@ def test_binding_names_match_header():
 
 
 def test_abi_version(lib):
-    assert lib.grok_abi_version() == 1
+    assert lib.grok_abi_version() == 2
 
 
 def test_workspace_size_is_host_only(lib):
     n = ctypes.c_size_t(0)
     s = ctypes.c_int(0)
     assert lib.grok_attn_decode_workspace(32, 8192, ctypes.byref(n), ctypes.byref(s)) == 0
-    assert s.value == 16
-    o_bytes = 32 * 8 * 16 * 6 * 128 * 4
-    l_bytes = 32 * 8 * 16 * 6 * 4
+    assert s.value == 8192 // 1024          # splits of GROK_DECODE_SPLIT = 1024 keys
+    o_bytes = 32 * 8 * 8 * 6 * 128 * 4
+    l_bytes = 32 * 8 * 8 * 6 * 4
     assert n.value == o_bytes + ((l_bytes + 255) // 256) * 256
     assert lib.grok_attn_decode_workspace(0, 8192, ctypes.byref(n), ctypes.byref(s)) == 1
     assert lib.grok_attn_decode_workspace(1, 70000, ctypes.byref(n), ctypes.byref(s)) == 1

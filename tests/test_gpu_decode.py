@@ -25,8 +25,9 @@ def test_decode_full_size_every_output():
 
 
 def test_decode_split_boundaries():
-    # kv_len = 1, 2, 512, 513, 1024, 2048: one row, split edges, a full cache
-    inp = W.custom(B=6, T=1, Tmax=2048, start_pos=[0, 1, 511, 512, 1023, 2047], seed=31)
+    # kv_len = 1, 2, 512, 513, 1023, 1024, 1025, 2048: one row, stage and split edges
+    # (a split is GROK_DECODE_SPLIT = 1024 rows), a full cache
+    inp = W.custom(B=8, T=1, Tmax=2048, start_pos=[0, 1, 511, 512, 1022, 1023, 1024, 2047], seed=31)
     _check(inp, "split edges")
 
 
@@ -69,7 +70,7 @@ def test_workspace_query_and_small_workspace_rejected():
     import torch
     import grok_gqa_attention_gb300 as G
     nbytes, splits = G.decode_workspace(32, 8192)
-    assert splits == 16 and nbytes >= 32 * 8 * 16 * (6 * 128 + 6) * 4
+    assert splits == 8192 // G.DECODE_SPLIT and nbytes >= 32 * 8 * splits * (6 * 128 + 6) * 4
     inp = W.custom(B=2, T=1, Tmax=1024, start_pos=[3, 4], seed=35)
     dev = "cuda"
     ck, cv = inp.cache_k.to(dev), inp.cache_v.to(dev)

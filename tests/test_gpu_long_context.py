@@ -1,7 +1,7 @@
 """Parity at the largest supported cache: 65536 positions (GROK_MAX_POSITION).
 
 A chunked prefill whose last token sits at the final position, a decode step
-over a full 65536-row cache (128 splits), and the same prefill through a
+over a full 65536-row cache (64 splits), and the same prefill through a
 512-page block table. Outputs are compared with the exact oracle: every
 output of the decode step, sampled rows of the prefill (each one a dot
 product against up to 65536 keys).

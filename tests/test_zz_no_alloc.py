@@ -88,9 +88,9 @@ def test_warm_static_call_allocates_no_device_memory():
 
 def test_static_workspace_rejects_shapes_beyond_its_size():
     G, lib = _lib()
-    nbytes, _ = G.decode_workspace(64, 8192)
+    nbytes, _ = G.decode_workspace(128, 8192)
     assert nbytes > 16 << 20
     n = ctypes.c_void_p(0)
-    rc = lib.grok_attn_decode_step_static(n, n, n, n, 64, 8192, n, n, n)
+    rc = lib.grok_attn_decode_step_static(n, n, n, n, 128, 8192, n, n, n)
     assert rc == 1
     assert b"static workspace" in lib.grok_last_error()
