@@ -39,6 +39,23 @@ def test_binding_names_match_header():
     assert sorted(G.EXPORTS) == _declared()
 
 
+def test_binding_constants_match_header():
+    """The binding's copies of the header's constants (sizes, split, status codes, device bits)."""
+    import grok_gqa_attention_gb300 as G
+    text = open(os.path.join(ROOT, "include", "grok_attn.h")).read()
+    defines = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"^#define (GROK_\w+) (0x[0-9a-fA-F]+|\d+)\b", text, re.M)}
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"^\s*(GROK_(?:OK|ERR_\w+)) = (\d+)", text, re.M)}
+    pairs = {"N_Q_HEADS": "GROK_N_Q_HEADS", "N_KV_HEADS": "GROK_N_KV_HEADS", "HEAD_DIM": "GROK_HEAD_DIM",
+             "DECODE_SPLIT": "GROK_DECODE_SPLIT", "MAX_POSITION": "GROK_MAX_POSITION", "PAGE_TOKENS": "GROK_PAGE_TOKENS",
+             "DEV_BAD_START": "GROK_DEV_BAD_START", "DEV_BAD_VALID": "GROK_DEV_BAD_VALID",
+             "DEV_BAD_KV_LEN": "GROK_DEV_BAD_KV_LEN", "DEV_TIMEOUT": "GROK_DEV_TIMEOUT", "DEV_BAD_PAGE": "GROK_DEV_BAD_PAGE"}
+    for py, c in pairs.items():
+        assert getattr(G, py) == defines[c], (py, c)
+    for py, c in {"OK": "GROK_OK", "ERR_INVALID_ARG": "GROK_ERR_INVALID_ARG", "ERR_UNSUPPORTED": "GROK_ERR_UNSUPPORTED",
+                  "ERR_CUDA": "GROK_ERR_CUDA", "ERR_DEVICE_FAULT": "GROK_ERR_DEVICE_FAULT"}.items():
+        assert getattr(G, py) == enums[c], (py, c)
+
+
 def test_abi_version(lib):
     assert lib.grok_abi_version() == 2
 
